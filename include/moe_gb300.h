@@ -1,0 +1,212 @@
+/*
+ * moe_gb300.h -- C ABI of the MoE expert block on one GB300 (sm_103a).
+ *
+ * The block has four steps, each a hand-written CUDA kernel (or a few):
+ *   route     per-token top-k over fp32 router logits, softmax over the k chosen;
+ *   dispatch  stable counting sort of the T*k (token, slot) assignments by expert,
+ *             copying each token row into its expert's contiguous segment;
+ *   experts   grouped SwiGLU MLPs over the segments on the tcgen05 tensor cores
+ *             (bf16 in, fp32 accumulate in TMEM);
+ *   combine   per-token gather of its k expert rows, weighted by the routing weights;
+ * plus the backward pass for dX, dW_gu and dW_down.
+ *
+ * Where the method is stated: "Halo's 2.8x over TRL is not a kernel, and its own
+ * benchmark proves it", section "Where the gap actually is" and its Figure 3 ("EP
+ * token routing": fp32 router logits, per-token top-k router, grouped matmul over
+ * tokens sorted by expert, rows returned in order weighted by the top-k
+ * probabilities); "Halo: Frontier-Lab Training for Everyone", sections "Novel model
+ * integration" (grouped GEMM with fused SwiGLU), "One trainer architecture" (fused
+ * experts as 3-D weight tensors) and "The hard problems along the way" (atomic-free
+ * routing backward; a fused SwiGLU kernel that overflowed at 745k tokens on one GPU,
+ * which is why every byte offset here is 64-bit).
+ *
+ * Conventions for every call:
+ *   - Shapes: T tokens, d hidden, E experts, k experts per token, f expert FFN width.
+ *     A = T*k assignments. All matrices are row-major and densely packed.
+ *   - Types: bf16 is IEEE bfloat16 passed as uint16_t bit patterns (moe_bf16);
+ *     router logits and routing weights are fp32; indices are int32.
+ *   - Pointers are DEVICE pointers owned by the caller unless stated. The library
+ *     allocates no device memory and keeps no per-call state; scratch lives in the
+ *     caller's workspace. Every pointer must be 16-byte aligned.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and return a status for errors the host can see: argument, shape,
+ *     alignment, workspace size, 32-bit index overflow, or a failed launch. Device
+ *     faults surface at the caller's next synchronisation. Nothing aborts the process.
+ *   - Preconditions checked on the host: 1 <= k <= min(E, 16), 1 <= E <= 256,
+ *     T >= 0, d >= 8 and f >= 8 with d % 8 == 0 and f % 8 == 0 (16-byte rows),
+ *     T*k and the padded row count below 2^31. Router logits must be finite
+ *     (not checked; the result for NaN/Inf logits is unspecified).
+ *
+ * Segment-padded row space. The dispatched rows (Xp, H, GU, O) live in a row space
+ * of R = moe_padded_rows(shape) rows where expert e's segment starts at row
+ *   P_e = 128 * sum_{e' < e} ceil(counts[e'] / 128)
+ * and holds its counts[e] rows in ascending token order (the stable sort), followed
+ * by zero rows up to the next multiple of 128. The compact layout of the method
+ * (segment e at offsets[e] = sum_{e'<e} counts[e']) is recovered as
+ *   compact row = row - P_e + offsets[e].
+ * Padding keeps every 128-row GEMM tile inside one expert.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;   /* IEEE bfloat16 bit pattern */
+typedef void *moe_stream;    /* cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* null pointer, bad shape or k > E */
+  MOE_ERR_UNSUPPORTED = -2,  /* shape outside the supported range (E > 256, k > 16, no sm_103 GPU) */
+  MOE_ERR_ALIGNMENT = -3,    /* a pointer is not 16-byte aligned, or d or f is not a multiple of 8 */
+  MOE_ERR_WORKSPACE = -4,    /* workspace or scratch smaller than the size query returns */
+  MOE_ERR_OVERFLOW = -5,     /* an index would not fit in int32 */
+  MOE_ERR_CUDA = -6,         /* a CUDA call or kernel launch failed */
+  MOE_ERR_TIMEOUT = -7       /* a kernel gave up waiting on its own pipeline (see moe_check_device_status) */
+} moe_status;
+
+typedef struct {
+  int64_t T; /* tokens */
+  int64_t d; /* hidden size */
+  int64_t E; /* experts */
+  int64_t k; /* experts per token */
+  int64_t f; /* expert FFN width: W_gu is E x d x 2f, W_down is E x f x d */
+} moe_shape;
+
+/* Text of a status code. Never NULL. */
+const char *moe_status_string(moe_status s);
+
+/* Rows R of the segment-padded row space (see above): 128 * (ceil(T*k/128) + E). */
+int64_t moe_padded_rows(moe_shape s);
+
+/* Bytes of the workspace that moe_forward (and any single-stage call) needs.
+ * training != 0 adds the saved pre-activations GU (R x 2f bf16) used by moe_backward. */
+size_t moe_workspace_size(moe_shape s, int training);
+
+/* Bytes of the scratch that moe_backward needs (G, dGU and dXp, R rows each). */
+size_t moe_backward_scratch_size(moe_shape s);
+
+/* Device pointers into a forward workspace, for callers that want the intermediate
+ * results of moe_forward. Layout is fixed by the shape and `training`.
+ * Fills every field; gu is NULL when training == 0. */
+typedef struct {
+  int32_t *ids;     /* T x k   chosen experts, slots in descending-logit order */
+  float *w;         /* T x k   routing weights (softmax over the k chosen logits) */
+  int32_t *counts;  /* E       rows per expert */
+  int32_t *offsets; /* E + 1   compact segment starts (exclusive prefix of counts) */
+  int32_t *padded_offsets; /* E + 1   segment starts P_e in the padded row space */
+  int32_t *row_of;  /* T x k   padded row of assignment (t, j) */
+  int32_t *tok_of;  /* R       token of each padded row, -1 on padding rows */
+  moe_bf16 *xp;     /* R x d   dispatched token rows */
+  moe_bf16 *gu;     /* R x 2f  gate|up pre-activations (training only) */
+  moe_bf16 *h;      /* R x f   SwiGLU activations */
+  moe_bf16 *o;      /* R x d   expert outputs */
+} moe_forward_views;
+moe_status moe_workspace_views(moe_shape s, int training, void *ws, size_t ws_bytes,
+                               moe_forward_views *out);
+
+/* Route. "Halo's 2.8x over TRL is not a kernel", Figure 3 and "Where the gap
+ * actually is": per-token top-k router on fp32 logits, outputs weighted by the
+ * top-k probabilities.
+ *   logits [T x E] fp32 in; ids [T x k] int32 out; w [T x k] fp32 out.
+ * ids[t][0..k-1] are the k experts with the largest logits, ordered by descending
+ * logit, equal logits by ascending expert index (the lower index wins a tie).
+ * w[t][j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen logits.
+ * One warp per token. No workspace. */
+moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w, moe_stream stream);
+
+/* Dispatch. Figure 3 of "Halo's 2.8x over TRL is not a kernel": tokens sorted by
+ * expert for a grouped matmul. A stable counting sort of the assignments
+ * a = t*k + j by ids: block histograms, an exclusive scan of the per-expert counts,
+ * and a 16-byte vectorised row scatter.
+ *   x [T x d] bf16 in; ids [T x k] int32 in (each row k distinct experts in [0, E));
+ *   xp [R x d] bf16 out (padding rows zeroed); counts [E], offsets [E+1] int32 out
+ *   (compact, offsets[E] = T*k); padded_offsets [E+1] int32 out (P_e);
+ *   row_of [T x k] int32 out (padded row of (t, j)); tok_of [R] int32 out (-1 on padding).
+ * Uses ws (at least moe_workspace_size(s, 0) bytes) for the block histograms. */
+moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xp,
+                        int32_t *counts, int32_t *offsets, int32_t *padded_offsets,
+                        int32_t *row_of, int32_t *tok_of, void *ws, size_t ws_bytes,
+                        moe_stream stream);
+
+/* Experts. "Halo: Frontier-Lab Training for Everyone", "Novel model integration":
+ * grouped GEMM with fused SwiGLU over 3-D expert weights. For every expert e and
+ * every row r of its segment:
+ *   gu = xp[r] @ W_gu[e]  (gate = columns [0, f), up = columns [f, 2f))
+ *   h[r] = silu(gate) * up,  o[r] = h[r] @ W_down[e]
+ * on tcgen05 tensor cores: bf16 operands, fp32 accumulation in TMEM, the SwiGLU in
+ * the epilogue of the first GEMM, h and o rounded to bf16 once.
+ *   xp [R x d] bf16 in, segment-padded as moe_dispatch writes it; counts [E] int32 in;
+ *   w_gu [E x d x 2f] bf16 in; w_down [E x f x d] bf16 in;
+ *   h [R x f] bf16 out; gu [R x 2f] bf16 out or NULL (saved for the backward);
+ *   o [R x d] bf16 out.
+ * Uses ws (at least moe_workspace_size(s, 0) bytes) for the tile plan. */
+moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts,
+                          const moe_bf16 *w_gu, const moe_bf16 *w_down, moe_bf16 *h,
+                          moe_bf16 *gu, moe_bf16 *o, void *ws, size_t ws_bytes,
+                          moe_stream stream);
+
+/* Combine. Figure 3 of "Halo's 2.8x over TRL is not a kernel": rows return to
+ * their token weighted by the top-k probabilities.
+ *   y[t] = bf16( sum_{j=0..k-1} w[t][j] * o[row_of[t][j]] ), an fp32 sum in slot
+ *   order, one rounding. A gather per token: deterministic, no atomics.
+ *   o [R x d] bf16 in; w [T x k] fp32 in; row_of [T x k] int32 in; y [T x d] bf16 out. */
+moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int32_t *row_of,
+                       moe_bf16 *y, moe_stream stream);
+
+/* The whole block: route, dispatch, experts, combine, with every intermediate in ws
+ * (see moe_workspace_views). training != 0 also keeps GU for moe_backward; ws must
+ * then hold moe_workspace_size(s, 1) bytes and outlive the matching moe_backward.
+ *   x [T x d] bf16; logits [T x E] fp32; w_gu [E x d x 2f] bf16; w_down [E x f x d] bf16;
+ *   y [T x d] bf16 out. */
+moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
+                       const moe_bf16 *w_down, moe_bf16 *y, int training, void *ws,
+                       size_t ws_bytes, moe_stream stream);
+
+/* Backward of the block for dY, the routing weights held constant ("Halo: Frontier-Lab
+ * Training for Everyone", "The hard problems along the way": an atomic-free routing
+ * backward). With G[r] = w[t][j] * dY[t] for r = row_of[t][j]:
+ *   dW_down[e] = H_e^T G_e;  dH = G W_down[e]^T;  dgate = dH * up * silu'(gate),
+ *   dup = dH * silu(gate);   dW_gu[e] = Xp_e^T [dgate | dup];
+ *   dXp = [dgate | dup] W_gu[e]^T;  dX[t] = sum_j dXp[row_of[t][j]] (a gather).
+ * Every gradient is written by exactly one thread (no atomics, bit-reproducible);
+ * experts with no rows get dW = 0.
+ *   dy [T x d] bf16 in; w_gu, w_down as in moe_forward; ws: the workspace of a
+ *   moe_forward(training = 1) call with the same shape and weights;
+ *   dx [T x d], dw_gu [E x d x 2f], dw_down [E x f x d] bf16 out;
+ *   scratch: at least moe_backward_scratch_size(s) bytes. */
+moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
+                        const moe_bf16 *w_down, const void *ws, size_t ws_bytes, moe_bf16 *dx,
+                        moe_bf16 *dw_gu, moe_bf16 *dw_down, void *scratch, size_t scratch_bytes,
+                        moe_stream stream);
+
+/* Device-side status of a workspace or scratch: synchronises `stream`, reads the
+ * status word that the kernels set when a pipeline wait runs past its time limit,
+ * and clears it. Returns MOE_OK or MOE_ERR_TIMEOUT. */
+moe_status moe_check_device_status(const void *ws_or_scratch, moe_stream stream);
+
+/* Launch timing for measurement. While enabled, the library brackets each kernel
+ * it launches with a pair of CUDA events recorded on that kernel's stream.
+ * moe_profile_stop synchronises those events and writes, for each launch in order,
+ * a static kernel name and its duration in milliseconds; it returns the number of
+ * launches recorded (at most `capacity` given to moe_profile_start) or a negative
+ * moe_status. Not thread-safe: for one host thread at a time. */
+typedef struct {
+  const char *name;
+  float ms;
+} moe_launch_time;
+moe_status moe_profile_start(int capacity);
+int moe_profile_stop(moe_launch_time *out, int out_capacity);
+
+/* Number of kernels the library has launched since it was loaded. */
+int64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,315 @@
+"""Python binding of libmoe_gb300.so, the C ABI of the MoE expert block on GB300.
+
+Argument marshalling only: every function checks tensor placement and dtypes,
+allocates the outputs and the workspace with torch (device memory is PyTorch's
+job here), and passes raw pointers plus the current CUDA stream to the C entry
+point of the same name. Every step of the block runs in the library's CUDA
+kernels; there is no fallback of any kind. If the library has not been built,
+or no GB300 is present, the calls raise.
+
+The C header (include/moe_gb300.h) documents each operation, its layout and its
+error behaviour; names and argument order here follow it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libmoe_gb300.so")
+
+_c_i64 = ctypes.c_int64
+_c_vp = ctypes.c_void_p
+
+
+class MoEShape(ctypes.Structure):
+    _fields_ = [("T", _c_i64), ("d", _c_i64), ("E", _c_i64), ("k", _c_i64), ("f", _c_i64)]
+
+
+class _Views(ctypes.Structure):
+    _fields_ = [(n, _c_vp) for n in ("ids", "w", "counts", "offsets", "padded_offsets", "row_of",
+                                     "tok_of", "xp", "gu", "h", "o")]
+
+
+class _LaunchTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("ms", ctypes.c_float)]
+
+
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
+          -3: "MOE_ERR_ALIGNMENT", -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_OVERFLOW",
+          -6: "MOE_ERR_CUDA", -7: "MOE_ERR_TIMEOUT"}
+
+# every exported entry point: (name, restype, argtypes)
+_SIG = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_padded_rows": (_c_i64, [MoEShape]),
+    "moe_workspace_size": (ctypes.c_size_t, [MoEShape, ctypes.c_int]),
+    "moe_backward_scratch_size": (ctypes.c_size_t, [MoEShape]),
+    "moe_workspace_views": (ctypes.c_int, [MoEShape, ctypes.c_int, _c_vp, ctypes.c_size_t,
+                                           ctypes.POINTER(_Views)]),
+    "moe_route": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "moe_dispatch": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                    _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_expert_ffn": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                      _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_combine": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "moe_forward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_int,
+                                   _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
+                                    _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_check_device_status": (ctypes.c_int, [_c_vp, _c_vp]),
+    "moe_profile_start": (ctypes.c_int, [ctypes.c_int]),
+    "moe_profile_stop": (ctypes.c_int, [ctypes.POINTER(_LaunchTime), ctypes.c_int]),
+    "moe_launch_count": (_c_i64, []),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_status_text(status)})")
+
+
+def _status_text(status: int) -> str:
+    try:
+        return lib().moe_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - the library itself may be what is missing
+        return "?"
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                "g.build()'); there is no non-CUDA path")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def shape(T: int, d: int, E: int, k: int, f: int) -> MoEShape:
+    return MoEShape(int(T), int(d), int(E), int(k), int(f))
+
+
+def _p(t: torch.Tensor | None) -> _c_vp:
+    if t is None:
+        return _c_vp(None)
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the MoE library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return _c_vp(t.data_ptr())
+
+
+def _stream() -> _c_vp:
+    return _c_vp(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(*ts: torch.Tensor) -> torch.device:
+    return next(t.device for t in ts if t is not None)
+
+
+def _want(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------------ sizes and views
+def padded_rows(s: MoEShape) -> int:
+    r = lib().moe_padded_rows(s)
+    if r < 0:
+        raise MoEError(-1, "moe_padded_rows")
+    return int(r)
+
+
+def workspace_size(s: MoEShape, training: bool) -> int:
+    n = lib().moe_workspace_size(s, int(bool(training)))
+    if n == 0:
+        raise MoEError(-1, "moe_workspace_size")
+    return int(n)
+
+
+def backward_scratch_size(s: MoEShape) -> int:
+    n = lib().moe_backward_scratch_size(s)
+    if n == 0:
+        raise MoEError(-1, "moe_backward_scratch_size")
+    return int(n)
+
+
+def new_workspace(s: MoEShape, training: bool, device="cuda") -> torch.Tensor:
+    return torch.empty(workspace_size(s, training), dtype=torch.uint8, device=device)
+
+
+def new_scratch(s: MoEShape, device="cuda") -> torch.Tensor:
+    return torch.empty(backward_scratch_size(s), dtype=torch.uint8, device=device)
+
+
+def workspace_views(s: MoEShape, training: bool, ws: torch.Tensor) -> dict:
+    """Tensor views of the intermediates a forward call leaves in its workspace."""
+    v = _Views()
+    _check(lib().moe_workspace_views(s, int(bool(training)), _p(ws), ws.numel(), ctypes.byref(v)),
+           "moe_workspace_views")
+    base = ws.data_ptr()
+    R = padded_rows(s)
+    T, d, E, k, f = s.T, s.d, s.E, s.k, s.f
+    spec = {"ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),
+            "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32),
+            "padded_offsets": ((E + 1,), torch.int32), "row_of": ((T, k), torch.int32),
+            "tok_of": ((R,), torch.int32), "xp": ((R, d), torch.bfloat16),
+            "gu": ((R, 2 * f), torch.bfloat16), "h": ((R, f), torch.bfloat16),
+            "o": ((R, d), torch.bfloat16)}
+    out = {}
+    for name, (shp, dt) in spec.items():
+        ptr = getattr(v, name)
+        if ptr is None:
+            out[name] = None
+            continue
+        off = ptr - base
+        n = 1
+        for x in shp:
+            n *= x
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        out[name] = ws[off:off + nbytes].view(dt).view(*shp)
+    return out
+
+
+# ------------------------------------------------------------------------- the stages
+def route(logits: torch.Tensor, k: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """moe_route: ids [T,k] int32, w [T,k] fp32."""
+    _want(logits, torch.float32, "logits")
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    s = shape(T, 8, E, k, 8)
+    _check(lib().moe_route(s, _p(logits), _p(ids), _p(w), _stream()), "moe_route")
+    return ids, w
+
+
+def dispatch(s: MoEShape, x: torch.Tensor, ids: torch.Tensor, ws: torch.Tensor | None = None) -> dict:
+    """moe_dispatch: the stable counting sort of the assignments by expert."""
+    _want(x, torch.bfloat16, "x")
+    _want(ids, torch.int32, "ids")
+    dev = x.device
+    R = padded_rows(s)
+    if ws is None:
+        ws = new_workspace(s, False, dev)
+    out = {"xp": torch.empty((R, s.d), dtype=torch.bfloat16, device=dev),
+           "counts": torch.empty((s.E,), dtype=torch.int32, device=dev),
+           "offsets": torch.empty((s.E + 1,), dtype=torch.int32, device=dev),
+           "padded_offsets": torch.empty((s.E + 1,), dtype=torch.int32, device=dev),
+           "row_of": torch.empty((s.T, s.k), dtype=torch.int32, device=dev),
+           "tok_of": torch.empty((R,), dtype=torch.int32, device=dev)}
+    _check(lib().moe_dispatch(s, _p(x), _p(ids), _p(out["xp"]), _p(out["counts"]),
+                              _p(out["offsets"]), _p(out["padded_offsets"]), _p(out["row_of"]),
+                              _p(out["tok_of"]), _p(ws), ws.numel(), _stream()), "moe_dispatch")
+    return out
+
+
+def expert_ffn(s: MoEShape, xp: torch.Tensor, counts: torch.Tensor, w_gu: torch.Tensor,
+               w_down: torch.Tensor, save_gu: bool = False, ws: torch.Tensor | None = None
+               ) -> tuple[torch.Tensor, torch.Tensor | None, torch.Tensor]:
+    """moe_expert_ffn: h [R,f], gu [R,2f] (if save_gu), o [R,d]."""
+    for t, n in ((xp, "xp"), (w_gu, "w_gu"), (w_down, "w_down")):
+        _want(t, torch.bfloat16, n)
+    _want(counts, torch.int32, "counts")
+    dev = xp.device
+    R = padded_rows(s)
+    if ws is None:
+        ws = new_workspace(s, False, dev)
+    h = torch.empty((R, s.f), dtype=torch.bfloat16, device=dev)
+    gu = torch.empty((R, 2 * s.f), dtype=torch.bfloat16, device=dev) if save_gu else None
+    o = torch.empty((R, s.d), dtype=torch.bfloat16, device=dev)
+    _check(lib().moe_expert_ffn(s, _p(xp), _p(counts), _p(w_gu), _p(w_down), _p(h), _p(gu), _p(o),
+                                _p(ws), ws.numel(), _stream()), "moe_expert_ffn")
+    return h, gu, o
+
+
+def combine(s: MoEShape, o: torch.Tensor, w: torch.Tensor, row_of: torch.Tensor) -> torch.Tensor:
+    """moe_combine: y [T,d] bf16."""
+    _want(o, torch.bfloat16, "o")
+    _want(w, torch.float32, "w")
+    _want(row_of, torch.int32, "row_of")
+    y = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=o.device)
+    _check(lib().moe_combine(s, _p(o), _p(w), _p(row_of), _p(y), _stream()), "moe_combine")
+    return y
+
+
+def forward(x: torch.Tensor, logits: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Tensor,
+            k: int, training: bool = False, ws: torch.Tensor | None = None,
+            y: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor, MoEShape]:
+    """moe_forward: returns (y, workspace, shape); the workspace feeds backward()."""
+    _want(x, torch.bfloat16, "x")
+    _want(logits, torch.float32, "logits")
+    T, d = x.shape
+    E, _, f2 = w_gu.shape
+    s = shape(T, d, E, k, f2 // 2)
+    if ws is None:
+        ws = new_workspace(s, training, x.device)
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_forward(s, _p(x), _p(logits), _p(w_gu), _p(w_down), _p(y), int(bool(training)),
+                             _p(ws), ws.numel(), _stream()), "moe_forward")
+    return y, ws, s
+
+
+def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Tensor,
+             ws: torch.Tensor, scratch: torch.Tensor | None = None,
+             out: tuple | None = None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """moe_backward: (dx, dw_gu, dw_down) for the forward that filled ws (training=True)."""
+    _want(dy, torch.bfloat16, "dy")
+    dev = dy.device
+    if scratch is None:
+        scratch = new_scratch(s, dev)
+    if out is None:
+        dx = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=dev)
+        dw_gu = torch.empty(tuple(w_gu.shape), dtype=torch.bfloat16, device=dev)
+        dw_down = torch.empty(tuple(w_down.shape), dtype=torch.bfloat16, device=dev)
+    else:
+        dx, dw_gu, dw_down = out
+    _check(lib().moe_backward(s, _p(dy), _p(w_gu), _p(w_down), _p(ws), ws.numel(), _p(dx),
+                              _p(dw_gu), _p(dw_down), _p(scratch), scratch.numel(), _stream()),
+           "moe_backward")
+    return dx, dw_gu, dw_down
+
+
+def check_device_status(ws_or_scratch: torch.Tensor) -> None:
+    _check(lib().moe_check_device_status(_p(ws_or_scratch), _stream()), "moe_check_device_status")
+
+
+# ------------------------------------------------------------------------ measurement
+def profile_start(capacity: int = 256) -> None:
+    _check(lib().moe_profile_start(int(capacity)), "moe_profile_start")
+
+
+def profile_stop(capacity: int = 4096) -> list[tuple[str, float]]:
+    buf = (_LaunchTime * capacity)()
+    n = lib().moe_profile_stop(buf, capacity)
+    if n < 0:
+        raise MoEError(n, "moe_profile_stop")
+    return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n, capacity))]
+
+
+def launch_count() -> int:
+    return int(lib().moe_launch_count())
+
+
+__all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
+           "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
+           "dispatch", "expert_ffn", "combine", "forward", "backward", "check_device_status",
+           "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

@@ -1,0 +1,585 @@
+// Grouped GEMM engine of the MoE expert block on the sm_103a tensor cores.
+//
+// The experts of "Halo: Frontier-Lab Training for Everyone" ("Novel model
+// integration": grouped GEMM with a fused SwiGLU; "One trainer architecture": fused
+// experts as 3-D weight tensors) run as one persistent kernel per GEMM over all
+// experts. Design:
+//   * one CTA per SM, 192 threads: warp 0 issues TMA loads, warp 1 issues
+//     tcgen05.mma (one elected lane), warps 2..5 run the epilogue out of TMEM;
+//   * tiles of 128 x 256 (M x N) with K steps of 64, 128-byte swizzled smem
+//     operands fed by cp.async.bulk.tensor into a 4-stage mbarrier ring;
+//   * the fp32 accumulator lives in TMEM, two 256-column buffers so the epilogue of
+//     one tile overlaps the main loop of the next;
+//   * ragged per-expert M: expert segments are padded to 128 rows, so every M tile
+//     belongs to one expert and a device-side table maps tile -> expert (no host
+//     sync, the schedule reads the routing result from device memory);
+//   * ragged per-expert K (weight gradients): the K loop runs over the expert's
+//     padded rows, whose padding is zero in both operands.
+// Every output element is written by exactly one thread; nothing uses atomics.
+#include "kernels.h"
+
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box (MN-major tiles are built of these)
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+
+enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
+
+struct Args {
+  const int32_t *padded;       // [E+1]
+  const int32_t *tile_expert;  // [R/128]
+  int E;
+  int n_tiles;  // tiles along N
+  int m_tiles;  // WGRAD: tiles along M of one expert's dW
+  int k_tiles;  // ragged-M kinds: K / 64, rounded up
+  int M_out;    // WGRAD: rows of dW[e]
+  int N_out;    // valid output columns
+  int f;        // SwiGLU width (GATE_UP, DGRAD_H)
+  void *out;
+  int64_t ld_out;
+  void *out2;   // GATE_UP: GU saved (or null)
+  int64_t ld_out2;
+  const void *aux;  // DGRAD_H: GU
+  int64_t ld_aux;
+  int *status;
+};
+
+struct Tile {
+  int e, m0, n0, kt, kr0;
+};
+
+template <int KIND>
+__device__ __forceinline__ int total_tiles(const Args &a) {
+  if (KIND == WGRAD) return a.E * a.m_tiles * a.n_tiles;
+  return (a.padded[a.E] / BM) * a.n_tiles;
+}
+
+template <int KIND>
+__device__ __forceinline__ Tile decode(const Args &a, int tile) {
+  Tile t;
+  if (KIND == WGRAD) {
+    const int per = a.m_tiles * a.n_tiles;
+    t.e = tile / per;
+    const int r = tile - t.e * per;
+    t.m0 = (r / a.n_tiles) * BM;
+    t.n0 = (r % a.n_tiles) * BN;
+    t.kr0 = a.padded[t.e];
+    t.kt = (a.padded[t.e + 1] - t.kr0) / BK;
+  } else {
+    const int mt = tile / a.n_tiles;
+    const int nt = tile - mt * a.n_tiles;
+    t.e = a.tile_expert[mt];
+    t.m0 = mt * BM;
+    t.n0 = nt * (KIND == GATE_UP ? BN / 2 : BN);
+    t.kt = a.k_tiles;
+    t.kr0 = 0;
+  }
+  return t;
+}
+
+template <int KIND>
+__device__ __forceinline__ void issue_loads(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                            uint8_t *sA, uint8_t *sB, uint64_t *bar,
+                                            const Tile &t, int kb) {
+  const int k0 = kb * BK;
+  // A operand
+  if (KIND == WGRAD) {
+    // X^T tile: columns m0..m0+127 of X, rows kr0+k0 .. +63 (MN-major)
+    tma_load_2d(sA, tmA, bar, t.m0, t.kr0 + k0);
+    tma_load_2d(sA + kBoxBytes, tmA, bar, t.m0 + 64, t.kr0 + k0);
+  } else {
+    tma_load_2d(sA, tmA, bar, k0, t.m0);  // rows m0..m0+127, K columns k0..k0+63
+  }
+  // B operand
+  if (KIND == GATE_UP) {
+    // W_gu viewed as [E][d][2][f]: gate columns n0..n0+127 then up columns n0..n0+127
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tma_load_4d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
+  } else if (KIND == DOWN) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_load_3d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * i, k0, t.e);
+  } else if (KIND == DGRAD_H || KIND == DGRAD_X) {
+    tma_load_3d(sB, tmB, bar, k0, t.n0, t.e);  // 256 N-rows x 64 K, K-major
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tma_load_2d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * i, t.kr0 + k0);
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
+
+__device__ __forceinline__ void store8(void *base, int64_t idx, const float (&v)[8]) {
+  *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(base) + idx) = pack8(v);
+}
+
+__device__ __forceinline__ void load8(const void *base, int64_t idx, float (&v)[8]) {
+  unpack8(*reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + idx), v);
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const Args &a, const Tile &t, uint32_t taddr,
+                                              int row_in_tile) {
+  if (KIND == GATE_UP) {
+    const int64_t row = t.m0 + row_in_tile;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+      float g[32], u[32];
+      tmem_ld32x2(taddr + c0, taddr + BN / 2 + c0, g, u);
+      const int col = t.n0 + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int c = col + 8 * v;
+        if (c < a.f) {
+          float h[8], gg[8], uu[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            gg[i] = g[8 * v + i];
+            uu[i] = u[8 * v + i];
+            h[i] = silu(gg[i]) * uu[i];
+          }
+          store8(a.out, row * a.ld_out + c, h);
+          if (a.out2) {
+            store8(a.out2, row * a.ld_out2 + c, gg);
+            store8(a.out2, row * a.ld_out2 + a.f + c, uu);
+          }
+        }
+      }
+    }
+  } else if (KIND == DOWN || KIND == DGRAD_X) {
+    const int64_t row = t.m0 + row_in_tile;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float acc[32];
+      tmem_ld32(taddr + c0, acc);
+      const int col = t.n0 + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int c = col + 8 * v;
+        if (c < a.N_out) {
+          float o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = acc[8 * v + i];
+          store8(a.out, row * a.ld_out + c, o);
+        }
+      }
+    }
+  } else if (KIND == DGRAD_H) {
+    const int64_t row = t.m0 + row_in_tile;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float dh[32];
+      tmem_ld32(taddr + c0, dh);
+      const int col = t.n0 + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int c = col + 8 * v;
+        if (c < a.f) {
+          float g[8], u[8], dg[8], du[8];
+          load8(a.aux, row * a.ld_aux + c, g);
+          load8(a.aux, row * a.ld_aux + a.f + c, u);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float s = 1.f / (1.f + __expf(-g[i]));
+            const float x = dh[8 * v + i];
+            dg[i] = x * u[i] * s * (1.f + g[i] * (1.f - s));
+            du[i] = x * g[i] * s;
+          }
+          store8(a.out, row * a.ld_out + c, dg);
+          store8(a.out, row * a.ld_out + a.f + c, du);
+        }
+      }
+    }
+  } else {  // WGRAD
+    const int m = t.m0 + row_in_tile;
+    const int64_t base = (int64_t)t.e * a.M_out * a.N_out + (int64_t)m * a.N_out;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float acc[32];
+      if (t.kt > 0) {
+        tmem_ld32(taddr + c0, acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      }
+      const int col = t.n0 + c0;
+      if (m < a.M_out) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int c = col + 8 * v;
+          if (c < a.N_out) {
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = acc[8 * v + i];
+            store8(a.out, base + c, o);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const Args a) {
+  constexpr int A_MN = (KIND == WGRAD) ? 1 : 0;
+  constexpr int B_MN = (KIND == DGRAD_H || KIND == DGRAD_X) ? 0 : 1;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  // descriptor strides: K-major SW128 tiles use SBO = 1024 (8 rows of 128 B) and step
+  // 32 B per 16-element K slice; MN-major SW128 tiles use LBO = one 64x64 box (the
+  // next 64 M/N columns), SBO = 1024 (8 K rows) and step 16 rows = 2048 B per K slice.
+  constexpr uint32_t kALbo = A_MN ? kBoxBytes : 16, kBLbo = B_MN ? kBoxBytes : 16;
+  constexpr uint32_t kAStep = A_MN ? 2048 : 32, kBStep = B_MN ? 2048 : 32;
+
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
+  __shared__ uint32_t tmem_slot;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    fence_barrier_init();
+    fence_proxy_async_shared();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  const int total = total_tiles<KIND>(a);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      int issued = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode<KIND>(a, tile);
+        for (int kb = 0; kb < t.kt; ++kb) {
+          if (!mbar_wait(&empty_bar[s], ph ^ 1, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sA = smem + s * kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+          issue_loads<KIND>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], t, kb);
+          ++issued;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // wait (bounded) for the copies this thread issued and that may be in flight
+        int n = issued < kStages ? issued : kStages;
+        int ss = s;
+        uint32_t pp = ph;
+        for (int i = 0; i < n; ++i) {
+          if (--ss < 0) {
+            ss = kStages - 1;
+            pp ^= 1;
+          }
+          mbar_wait(&full_bar[ss], pp, nullptr, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      int s = 0;
+      uint32_t ph = 0;
+      int buf = 0;
+      uint32_t aph = 0;
+      bool ok = true, any = false;
+      const uint32_t smem_base = smem_u32(smem);
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode<KIND>(a, tile);
+        if (!mbar_wait(&acce_bar[buf], aph ^ 1, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        if (t.kt == 0) {
+          mbar_arrive(&accf_bar[buf]);
+        } else {
+          for (int kb = 0; kb < t.kt; ++kb) {
+            if (!mbar_wait(&full_bar[s], ph, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_base + s * kStageBytes;
+            const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
+              const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+            }
+            any = true;
+            tc_commit(&empty_bar[s]);
+            if (++s == kStages) {
+              s = 0;
+              ph ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&accf_bar[buf]);
+        }
+        buf ^= 1;
+        if (buf == 0) aph ^= 1;
+      }
+      if (!ok && any) {
+        // let every issued MMA finish before the accumulator is freed
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int buf = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode<KIND>(a, tile);
+      bool ok = mbar_wait(&accf_bar[buf], aph, a.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+      epilogue_tile<KIND>(a, t, taddr, row_in_tile);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[buf]);
+      buf ^= 1;
+      if (buf == 0) aph ^= 1;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap &tmA, const CUtensorMap &tmB, const Args &a,
+                        int64_t max_tiles, const char *name, cudaStream_t st) {
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev & 63] = true;
+  }
+  if (max_tiles <= 0) return cudaSuccess;
+  const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
+  launch_begin(st);
+  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+  return note_launch(name, st);
+}
+
+inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+cudaError_t map2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  const uint64_t dims[2] = {inner, rows};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_inner, box_rows};
+  return encode_tensor_map(m, base, 2, dims, strides, box);
+}
+
+cudaError_t map3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_mid) {
+  const uint64_t dims[3] = {inner, mid, outer};
+  const uint64_t strides[2] = {inner * 2, inner * mid * 2};
+  const uint32_t box[3] = {box_inner, box_mid, 1};
+  return encode_tensor_map(m, base, 3, dims, strides, box);
+}
+
+Args base_args(const GemmPlan &p, int *status) {
+  Args a{};
+  a.padded = p.padded;
+  a.tile_expert = p.tile_expert;
+  a.E = p.E;
+  a.status = status;
+  return a;
+}
+
+}  // namespace
+
+cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                              const uint64_t *strides_bytes, const uint32_t *box) {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return cudaErrorNotSupported;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i < rank - 1) gstride[i] = strides_bytes[i];
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                        const_cast<void *>(base), gdim, gstride, bdim, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &c = cache[dev & 63];
+  if (c == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    c = n > 0 ? n : 1;
+  }
+  return c;
+}
+
+cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, void *h, void *gu,
+                         int d, int f, int *status, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  cudaError_t e = map2d(&tA, xp, d, p.R, 64, BM);
+  if (e != cudaSuccess) return e;
+  {
+    const uint64_t dims[4] = {(uint64_t)f, 2, (uint64_t)d, (uint64_t)p.E};
+    const uint64_t strides[3] = {(uint64_t)f * 2, (uint64_t)f * 4, (uint64_t)d * f * 4};
+    const uint32_t box[4] = {64, 1, 64, 1};
+    e = encode_tensor_map(&tB, w_gu, 4, dims, strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  Args a = base_args(p, status);
+  a.n_tiles = cdiv(f, BN / 2);
+  a.k_tiles = cdiv(d, BK);
+  a.N_out = f;
+  a.f = f;
+  a.out = h;
+  a.ld_out = f;
+  a.out2 = gu;
+  a.ld_out2 = 2 * (int64_t)f;
+  return launch_kind<GATE_UP>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_gate_up_swiglu", st);
+}
+
+cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void *o, int d, int f,
+                      int *status, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  cudaError_t e = map2d(&tA, h, f, p.R, 64, BM);
+  if (e != cudaSuccess) return e;
+  e = map3d(&tB, w_down, d, f, p.E, 64, 64);
+  if (e != cudaSuccess) return e;
+  Args a = base_args(p, status);
+  a.n_tiles = cdiv(d, BN);
+  a.k_tiles = cdiv(f, BK);
+  a.N_out = d;
+  a.out = o;
+  a.ld_out = d;
+  return launch_kind<DOWN>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_down", st);
+}
+
+cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, const void *gu,
+                         void *dgu, int d, int f, int *status, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  cudaError_t e = map2d(&tA, g, d, p.R, 64, BM);
+  if (e != cudaSuccess) return e;
+  e = map3d(&tB, w_down, d, f, p.E, 64, BN);  // [E][f][d]: K = d inner, N = f rows
+  if (e != cudaSuccess) return e;
+  Args a = base_args(p, status);
+  a.n_tiles = cdiv(f, BN);
+  a.k_tiles = cdiv(d, BK);
+  a.N_out = f;
+  a.f = f;
+  a.out = dgu;
+  a.ld_out = 2 * (int64_t)f;
+  a.aux = gu;
+  a.ld_aux = 2 * (int64_t)f;
+  return launch_kind<DGRAD_H>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_h_swiglu_bwd", st);
+}
+
+cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, void *dxp, int d,
+                         int f, int *status, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  cudaError_t e = map2d(&tA, dgu, 2 * (uint64_t)f, p.R, 64, BM);
+  if (e != cudaSuccess) return e;
+  e = map3d(&tB, w_gu, 2 * (uint64_t)f, d, p.E, 64, BN);  // [E][d][2f]: K = 2f inner, N = d rows
+  if (e != cudaSuccess) return e;
+  Args a = base_args(p, status);
+  a.n_tiles = cdiv(d, BN);
+  a.k_tiles = cdiv(2 * (int64_t)f, BK);
+  a.N_out = d;
+  a.out = dxp;
+  a.ld_out = d;
+  return launch_kind<DGRAD_X>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_x", st);
+}
+
+cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
+                       int *status, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  cudaError_t e = map2d(&tA, x, M, p.R, 64, 64);
+  if (e != cudaSuccess) return e;
+  e = map2d(&tB, y, N, p.R, 64, 64);
+  if (e != cudaSuccess) return e;
+  Args a = base_args(p, status);
+  a.m_tiles = cdiv(M, BM);
+  a.n_tiles = cdiv(N, BN);
+  a.M_out = M;
+  a.N_out = N;
+  a.out = dw;
+  return launch_kind<WGRAD>(tA, tB, a, (int64_t)p.E * a.m_tiles * a.n_tiles, "gemm_wgrad", st);
+}
+
+}  // namespace moe

@@ -1,0 +1,81 @@
+// Internal interface between the C-ABI layer (moe_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kTileRows = 128;  // rows of one GEMM tile; expert segments are padded to it
+
+// Launch bookkeeping (moe_api.cu): launch_begin() before a kernel launch records a
+// start event when profiling is on; note_launch() after it records the end event,
+// counts the launch and returns cudaGetLastError().
+void launch_begin(cudaStream_t st);
+cudaError_t note_launch(const char *name, cudaStream_t st);
+
+// route_dispatch.cu
+cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *rank,
+                         int32_t *hist, int T, int E, int k, bool with_count, cudaStream_t st);
+cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,
+                         cudaStream_t st);
+cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
+                        int32_t *padded, int32_t *tile_expert, cudaStream_t st);
+cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t *padded,
+                        int32_t *tile_expert, cudaStream_t st);
+cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *rank,
+                           const int32_t *hist, const int32_t *padded, const int32_t *counts,
+                           int32_t *row_of, int32_t *tok_of, void *xp, int T, int d, int E, int k,
+                           cudaStream_t st);
+cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of, void *y, int T,
+                           int d, int k, cudaStream_t st);
+cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, int T, int d,
+                              int k, cudaStream_t st);
+cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *row_of,
+                                 const int32_t *padded, const int32_t *counts, void *g, int T,
+                                 int d, int E, int k, cudaStream_t st);
+
+// grouped_gemm.cu -- the tcgen05 grouped GEMM engine.
+//
+// Ragged-M problems (one per expert, rows = the expert's padded segment):
+//   GATE_UP   : H = swiglu(Xp W_gu[e]) [+ GU saved]      A = Xp   [R x d]   K-major
+//                                                        B = W_gu [E x d x 2f] MN-major
+//   DOWN      : O = H W_down[e]                          A = H    [R x f]   K-major
+//                                                        B = W_down [E x f x d] MN-major
+//   DGRAD_H   : dGU = swiglu_bwd(G W_down[e]^T, GU)      A = G    [R x d]   K-major
+//                                                        B = W_down [E x f x d] K-major
+//   DGRAD_X   : dXp = dGU W_gu[e]^T                      A = dGU  [R x 2f]  K-major
+//                                                        B = W_gu [E x d x 2f] K-major
+// Ragged-K problems (one per expert, K = the expert's padded segment):
+//   WGRAD     : dW[e] = X_e^T Y_e                        A = X [R x M] MN-major
+//                                                        B = Y [R x N] MN-major
+struct GemmPlan {
+  const int32_t *padded;       // [E+1] padded segment starts
+  const int32_t *tile_expert;  // [R/128] expert of each 128-row tile
+  int E;
+  int64_t R;                   // rows of the padded space
+};
+
+cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, void *h, void *gu,
+                         int d, int f, int *status, cudaStream_t st);
+cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void *o, int d, int f,
+                      int *status, cudaStream_t st);
+cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, const void *gu,
+                         void *dgu, int d, int f, int *status, cudaStream_t st);
+cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, void *dxp, int d,
+                         int f, int *status, cudaStream_t st);
+// dW[e] (M x N, bf16, row-major, experts contiguous) = X_e^T Y_e over the padded
+// segment rows of expert e; X is R x M, Y is R x N.
+cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
+                       int *status, cudaStream_t st);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved once).
+cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                              const uint64_t *strides_bytes, const uint32_t *box);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,391 @@
+// C ABI of the MoE expert block: argument checks, workspace layout, and the launch
+// sequences of each entry point. The arithmetic is in route_dispatch.cu and
+// grouped_gemm.cu; this file only validates, carves workspaces and orders launches.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/moe_gb300.h"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct FwdLayout {
+  size_t status, ids, w, rank, hist, counts, offsets, padded, tile_expert, row_of, tok_of, xp, gu,
+      h, o, total;
+};
+
+struct BwdLayout {
+  size_t status, g, dgu, dxp, total;
+};
+
+int64_t padded_rows(const moe_shape &s) {
+  const int64_t A = s.T * s.k;
+  return (int64_t)kTileRows * ((A + kTileRows - 1) / kTileRows + s.E);
+}
+
+FwdLayout fwd_layout(const moe_shape &s, int training) {
+  FwdLayout L{};
+  const int64_t A = s.T * s.k, R = padded_rows(s);
+  const int64_t C = (s.T + 31) / 32 > 0 ? (s.T + 31) / 32 : 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L.status = take(kAlign);
+  L.ids = take(A * 4);
+  L.w = take(A * 4);
+  L.rank = take(A * 4);
+  L.hist = take((size_t)s.E * C * 4);
+  L.counts = take(s.E * 4);
+  L.offsets = take((s.E + 1) * 4);
+  L.padded = take((s.E + 1) * 4);
+  L.tile_expert = take(R / kTileRows * 4);
+  L.row_of = take(A * 4);
+  L.tok_of = take(R * 4);
+  L.xp = take((size_t)R * s.d * 2);
+  L.gu = training ? take((size_t)R * 2 * s.f * 2) : 0;
+  L.h = take((size_t)R * s.f * 2);
+  L.o = take((size_t)R * s.d * 2);
+  L.total = off;
+  return L;
+}
+
+BwdLayout bwd_layout(const moe_shape &s) {
+  BwdLayout L{};
+  const int64_t R = padded_rows(s);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L.status = take(kAlign);
+  L.g = take((size_t)R * s.d * 2);
+  L.dgu = take((size_t)R * 2 * s.f * 2);
+  L.dxp = take((size_t)R * s.d * 2);
+  L.total = off;
+  return L;
+}
+
+moe_status check_shape(const moe_shape &s) {
+  if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.f <= 0) return MOE_ERR_INVALID_ARG;
+  if (s.k > s.E) return MOE_ERR_INVALID_ARG;
+  if (s.E > 256 || s.k > 16) return MOE_ERR_UNSUPPORTED;
+  if (s.d % 8 != 0 || s.f % 8 != 0) return MOE_ERR_ALIGNMENT;
+  if (s.d > (1 << 20) || s.f > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  const int64_t lim = (int64_t)1 << 31;
+  if (s.T >= lim / s.k) return MOE_ERR_OVERFLOW;            // T*k fits int32
+  if (padded_rows(s) >= lim) return MOE_ERR_OVERFLOW;       // padded rows fit int32
+  return MOE_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <typename... P>
+moe_status check_ptrs(P... ptrs) {
+  const void *a[] = {static_cast<const void *>(ptrs)...};
+  for (const void *p : a) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+moe_status check_device() {
+  static int ok[64] = {};  // 0 unknown, 1 good, -1 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int &v = ok[dev & 63];
+  if (v == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    v = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return v == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                   \
+  do {                                  \
+    const moe_status _s = (expr);       \
+    if (_s != MOE_OK) return _s;        \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+template <typename T>
+T *at(void *base, size_t off) {
+  return reinterpret_cast<T *>(static_cast<uint8_t *>(base) + off);
+}
+
+// ----------------------------------------------------------------- profiling state
+std::atomic<int64_t> g_launches{0};
+struct Prof {
+  bool on = false;
+  int cap = 0, used = 0;
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<const char *> names;
+  bool pending = false;
+} g_prof;
+
+}  // namespace
+
+namespace moe {
+
+void launch_begin(cudaStream_t st) {
+  if (g_prof.on && g_prof.used < g_prof.cap) {
+    cudaEventRecord(g_prof.start[g_prof.used], st);
+    g_prof.pending = true;
+  }
+}
+
+cudaError_t note_launch(const char *name, cudaStream_t st) {
+  const cudaError_t e = cudaGetLastError();
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_prof.on && g_prof.pending) {
+    cudaEventRecord(g_prof.stop[g_prof.used], st);
+    g_prof.names[g_prof.used] = name;
+    ++g_prof.used;
+    g_prof.pending = false;
+  }
+  return e;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer or dimension";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_OVERFLOW: return "index overflow";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+int64_t moe_padded_rows(moe_shape s) {
+  if (check_shape(s) != MOE_OK) return -1;
+  return padded_rows(s);
+}
+
+size_t moe_workspace_size(moe_shape s, int training) {
+  if (check_shape(s) != MOE_OK) return 0;
+  return fwd_layout(s, training).total;
+}
+
+size_t moe_backward_scratch_size(moe_shape s) {
+  if (check_shape(s) != MOE_OK) return 0;
+  return bwd_layout(s).total;
+}
+
+moe_status moe_workspace_views(moe_shape s, int training, void *ws, size_t ws_bytes,
+                               moe_forward_views *out) {
+  MOE_TRY(check_shape(s));
+  if (!ws || !out) return MOE_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(s, training);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  out->ids = at<int32_t>(ws, L.ids);
+  out->w = at<float>(ws, L.w);
+  out->counts = at<int32_t>(ws, L.counts);
+  out->offsets = at<int32_t>(ws, L.offsets);
+  out->padded_offsets = at<int32_t>(ws, L.padded);
+  out->row_of = at<int32_t>(ws, L.row_of);
+  out->tok_of = at<int32_t>(ws, L.tok_of);
+  out->xp = at<moe_bf16>(ws, L.xp);
+  out->gu = training ? at<moe_bf16>(ws, L.gu) : nullptr;
+  out->h = at<moe_bf16>(ws, L.h);
+  out->o = at<moe_bf16>(ws, L.o);
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(logits, ids, w));
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_route(logits, ids, w, nullptr, nullptr, (int)s.T, (int)s.E, (int)s.k, false,
+                        st));
+  return MOE_OK;
+}
+
+moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xp,
+                        int32_t *counts, int32_t *offsets, int32_t *padded_offsets,
+                        int32_t *row_of, int32_t *tok_of, void *ws, size_t ws_bytes,
+                        moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(xp, counts, offsets, padded_offsets, tok_of, ws));
+  if (s.T > 0) MOE_TRY(check_ptrs(x, ids, row_of));
+  const FwdLayout L = fwd_layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d;
+  int32_t *rank = at<int32_t>(ws, L.rank), *hist = at<int32_t>(ws, L.hist);
+  MOE_CUDA(launch_count(ids, rank, hist, T, E, k, st));
+  MOE_CUDA(launch_scan(hist, T, E, counts, offsets, padded_offsets, at<int32_t>(ws, L.tile_expert),
+                       st));
+  MOE_CUDA(launch_scatter(x, ids, rank, hist, padded_offsets, counts, row_of, tok_of, xp, T, d, E,
+                          k, st));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts,
+                          const moe_bf16 *w_gu, const moe_bf16 *w_down, moe_bf16 *h,
+                          moe_bf16 *gu, moe_bf16 *o, void *ws, size_t ws_bytes,
+                          moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(xp, counts, w_gu, w_down, h, o, ws));
+  if (gu && !aligned16(gu)) return MOE_ERR_ALIGNMENT;
+  const FwdLayout L = fwd_layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int *status = at<int>(ws, L.status);
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
+  MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, st));
+  const GemmPlan p{padded, tiles, (int)s.E, padded_rows(s)};
+  MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, (int)s.d, (int)s.f, status, st));
+  MOE_CUDA(gemm_down(p, h, w_down, o, (int)s.d, (int)s.f, status, st));
+  return MOE_OK;
+}
+
+moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int32_t *row_of,
+                       moe_bf16 *y, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(o, w, row_of, y));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_combine(o, w, row_of, y, (int)s.T, (int)s.d, (int)s.k,
+                          static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
+                       const moe_bf16 *w_down, moe_bf16 *y, int training, void *ws,
+                       size_t ws_bytes, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(w_gu, w_down, ws));
+  if (s.T > 0) MOE_TRY(check_ptrs(x, logits, y));
+  const FwdLayout L = fwd_layout(s, training);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d, f = (int)s.f;
+  int *status = at<int>(ws, L.status);
+  int32_t *ids = at<int32_t>(ws, L.ids), *rank = at<int32_t>(ws, L.rank);
+  int32_t *hist = at<int32_t>(ws, L.hist), *counts = at<int32_t>(ws, L.counts);
+  int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
+  int32_t *row_of = at<int32_t>(ws, L.row_of), *tok_of = at<int32_t>(ws, L.tok_of);
+  float *w = at<float>(ws, L.w);
+  void *xp = at<void>(ws, L.xp), *h = at<void>(ws, L.h), *o = at<void>(ws, L.o);
+  void *gu = training ? at<void>(ws, L.gu) : nullptr;
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOE_CUDA(launch_route(logits, ids, w, rank, hist, T, E, k, true, st));
+  MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, st));
+  MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k, st));
+  const GemmPlan p{padded, tiles, E, padded_rows(s)};
+  MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
+  MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));
+  MOE_CUDA(launch_combine(o, w, row_of, y, T, d, k, st));
+  return MOE_OK;
+}
+
+moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
+                        const moe_bf16 *w_down, const void *ws, size_t ws_bytes, moe_bf16 *dx,
+                        moe_bf16 *dw_gu, moe_bf16 *dw_down, void *scratch, size_t scratch_bytes,
+                        moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(w_gu, w_down, ws, dw_gu, dw_down, scratch));
+  if (s.T > 0) MOE_TRY(check_ptrs(dy, dx));
+  const FwdLayout L = fwd_layout(s, 1);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const BwdLayout B = bwd_layout(s);
+  if (scratch_bytes < B.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d, f = (int)s.f;
+  void *fws = const_cast<void *>(ws);
+  const float *w = at<float>(fws, L.w);
+  const int32_t *row_of = at<int32_t>(fws, L.row_of), *counts = at<int32_t>(fws, L.counts);
+  const int32_t *padded = at<int32_t>(fws, L.padded), *tiles = at<int32_t>(fws, L.tile_expert);
+  const void *xp = at<void>(fws, L.xp), *gu = at<void>(fws, L.gu), *h = at<void>(fws, L.h);
+  int *status = at<int>(scratch, B.status);
+  void *g = at<void>(scratch, B.g), *dgu = at<void>(scratch, B.dgu), *dxp = at<void>(scratch, B.dxp);
+  const GemmPlan p{padded, tiles, E, padded_rows(s)};
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, st));
+  MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));
+  MOE_CUDA(gemm_wgrad(p, h, g, dw_down, f, d, status, st));
+  MOE_CUDA(gemm_dgrad_x(p, dgu, w_gu, dxp, d, f, status, st));
+  MOE_CUDA(gemm_wgrad(p, xp, dgu, dw_gu, d, 2 * f, status, st));
+  MOE_CUDA(launch_gather_sum(dxp, row_of, dx, T, d, k, st));
+  return MOE_OK;
+}
+
+moe_status moe_check_device_status(const void *ws_or_scratch, moe_stream stream) {
+  if (!ws_or_scratch) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  MOE_CUDA(cudaMemcpyAsync(&v, ws_or_scratch, sizeof(int), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaStreamSynchronize(st));
+  if (v != kDevOk) {
+    MOE_CUDA(cudaMemsetAsync(const_cast<void *>(ws_or_scratch), 0, sizeof(int), st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    return MOE_ERR_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_profile_start(int capacity) {
+  if (capacity <= 0) return MOE_ERR_INVALID_ARG;
+  for (cudaEvent_t e : g_prof.start) cudaEventDestroy(e);
+  for (cudaEvent_t e : g_prof.stop) cudaEventDestroy(e);
+  g_prof = Prof{};
+  g_prof.start.resize(capacity);
+  g_prof.stop.resize(capacity);
+  g_prof.names.resize(capacity);
+  for (int i = 0; i < capacity; ++i) {
+    if (cudaEventCreate(&g_prof.start[i]) != cudaSuccess ||
+        cudaEventCreate(&g_prof.stop[i]) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  g_prof.cap = capacity;
+  g_prof.on = true;
+  return MOE_OK;
+}
+
+int moe_profile_stop(moe_launch_time *out, int out_capacity) {
+  if (!g_prof.on) return 0;
+  g_prof.on = false;
+  const int n = g_prof.used;
+  for (int i = 0; i < n && i < out_capacity; ++i) {
+    if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    out[i].name = g_prof.names[i];
+    out[i].ms = ms;
+  }
+  return n;
+}
+
+int64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

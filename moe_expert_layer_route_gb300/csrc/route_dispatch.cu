@@ -1,0 +1,432 @@
+// Bandwidth-bound stages of the MoE expert block: route, dispatch (histogram, scan,
+// scatter), combine, and the two backward gathers.
+//
+// Route and combine follow Figure 3 ("EP token routing") of "Halo's 2.8x over TRL
+// is not a kernel, and its own benchmark proves it": a per-token top-k router on
+// fp32 logits, a grouped matmul over tokens sorted by expert, and rows returned to
+// their token weighted by the top-k probabilities. Every output element here is
+// written by one thread and every sum runs in a fixed order, so results are
+// bit-reproducible without atomics ("The hard problems along the way" in "Halo:
+// Frontier-Lab Training for Everyone" credits an atomic-free routing backward).
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kChunk = 32;        // tokens per histogram chunk (one per lane of a warp)
+constexpr int kMaxK = 16;
+constexpr int kMaxE = 256;
+
+// ---------------------------------------------------------------------------- route
+// One warp per token. Lane l holds logits l, l+32, ... (E <= 256, so <= 8 each).
+// k rounds of a warp arg-max under the order (logit descending, index ascending);
+// lane j keeps slot j. Weights: softmax over the k chosen logits in fp32.
+__device__ __forceinline__ void route_one_token(const float *__restrict__ row, int E, int k,
+                                                int lane, int &slot_id, float &slot_w) {
+  float v[8];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    v[q] = (e < E) ? __ldg(row + e) : 0.f;
+    if (e >= E) taken |= 1u << q;
+  }
+  float my_v = 0.f;
+  int my_i = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.f;
+    int bi = 0x7fffffff;  // "none"
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!((taken >> q) & 1u)) {
+        // candidates in ascending index: strict '>' keeps the lower index on ties
+        if (bi == 0x7fffffff || v[q] > bv) {
+          bv = v[q];
+          bi = lane + 32 * q;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      const bool better = (oi != 0x7fffffff) &&
+                          (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+      if (better) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float z = (lane < k) ? expf(my_v - m) : 0.f;
+  float s = z;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  slot_id = my_i;
+  slot_w = z / s;
+}
+
+// Ballot count of one chunk of 32 tokens: for each expert, the number of tokens of
+// the chunk that chose it (hist[e][c]) and, for each (token, slot), the number of
+// earlier tokens of the chunk that chose the same expert (the stable local rank).
+__device__ __forceinline__ void count_chunk(const int32_t (*s_ids)[kMaxK], int c, int T, int E,
+                                            int k, int C, int warp, int nwarps, int lane,
+                                            int32_t *__restrict__ rank,
+                                            int32_t *__restrict__ hist) {
+  const int t = c * kChunk + lane;
+  const bool valid = t < T;
+  for (int e = warp; e < E; e += nwarps) {
+    int slot = -1;
+    if (valid) {
+      for (int j = 0; j < k; ++j)
+        if (s_ids[lane][j] == e) slot = j;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, slot >= 0);
+    if (slot >= 0) rank[(int64_t)t * k + slot] = __popc(m & lanemask_lt());
+    if (lane == 0) hist[(int64_t)e * C + c] = __popc(m);
+  }
+}
+
+// Block c routes tokens [32c, 32c+32) with 8 warps and, when COUNT, also writes the
+// chunk histogram and local ranks for the dispatch.
+template <bool COUNT>
+__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits,
+                                                    int32_t *__restrict__ ids,
+                                                    float *__restrict__ w,
+                                                    int32_t *__restrict__ rank,
+                                                    int32_t *__restrict__ hist, int T, int E,
+                                                    int k, int C) {
+  __shared__ int32_t s_ids[kChunk][kMaxK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  for (int i = warp; i < kChunk; i += 8) {
+    const int t = c * kChunk + i;
+    if (t >= T) break;
+    int sid;
+    float sw;
+    route_one_token(logits + (int64_t)t * E, E, k, lane, sid, sw);
+    if (lane < k) {
+      ids[(int64_t)t * k + lane] = sid;
+      w[(int64_t)t * k + lane] = sw;
+      s_ids[i][lane] = sid;
+    }
+  }
+  if constexpr (COUNT) {
+    __syncthreads();
+    count_chunk(s_ids, c, T, E, k, C, warp, 8, lane, rank, hist);
+  }
+}
+
+// Histogram and local ranks from ids already in memory (standalone dispatch).
+__global__ void __launch_bounds__(256) count_kernel(const int32_t *__restrict__ ids,
+                                                    int32_t *__restrict__ rank,
+                                                    int32_t *__restrict__ hist, int T, int E,
+                                                    int k, int C) {
+  __shared__ int32_t s_ids[kChunk][kMaxK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  for (int i = threadIdx.x; i < kChunk * k; i += blockDim.x) {
+    const int t = c * kChunk + i / k;
+    s_ids[i / k][i % k] = (t < T) ? ids[(int64_t)t * k + i % k] : -1;
+  }
+  __syncthreads();
+  count_chunk(s_ids, c, T, E, k, C, warp, 8, lane, rank, hist);
+}
+
+// --------------------------------------------------------------------------- scan
+// One block. Warp w scans the chunk counts of experts w, w+32, ... in chunk order,
+// turning hist[e][c] into the exclusive prefix within expert e; then the per-expert
+// totals give counts, compact offsets, padded offsets (segments rounded up to whole
+// 128-row tiles) and the table of which expert owns each 128-row tile.
+__device__ void plan_from_counts(const int32_t *s_cnt, int E, int32_t *__restrict__ offsets,
+                                 int32_t *__restrict__ padded, int32_t *__restrict__ tile_expert,
+                                 int32_t *s_pad) {
+  if (threadIdx.x == 0) {
+    int32_t off = 0, pad = 0;
+    for (int e = 0; e < E; ++e) {
+      offsets[e] = off;
+      padded[e] = pad;
+      s_pad[e] = pad;
+      off += s_cnt[e];
+      pad += (s_cnt[e] + kTileRows - 1) / kTileRows * kTileRows;
+    }
+    offsets[E] = off;
+    padded[E] = pad;
+    s_pad[E] = pad;
+  }
+  __syncthreads();
+  const int ntiles = s_pad[E] / kTileRows;
+  for (int mt = threadIdx.x; mt < ntiles; mt += blockDim.x) {
+    const int row = mt * kTileRows;
+    int lo = 0, hi = E - 1;  // last e with s_pad[e] <= row
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pad[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    tile_expert[mt] = lo;
+  }
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, int C, int E,
+                                                    int32_t *__restrict__ counts,
+                                                    int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ padded,
+                                                    int32_t *__restrict__ tile_expert) {
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_pad[kMaxE + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += 32) {
+    int32_t running = 0;
+    int32_t *h = hist + (int64_t)e * C;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+      const int c = c0 + lane;
+      const int32_t v = (c < C) ? h[c] : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < C) h[c] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_cnt[e] = running;
+      counts[e] = running;
+    }
+  }
+  __syncthreads();
+  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, s_pad);
+}
+
+// The same plan from counts alone (standalone expert FFN calls).
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ counts, int E,
+                                                    int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ padded,
+                                                    int32_t *__restrict__ tile_expert) {
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_pad[kMaxE + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = counts[e];
+  __syncthreads();
+  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, s_pad);
+}
+
+// ------------------------------------------------------------------------- scatter
+// Blocks [0, token_blocks): one warp per token; lane j < k computes the padded row of
+// slot j (segment start + chunk base + local rank), then the warp copies x[t] to each
+// of its k rows in 16-byte vectors (read once, written k times).
+// Blocks [token_blocks, token_blocks + E): block e zeroes expert e's padding rows.
+__global__ void __launch_bounds__(256) scatter_kernel(
+    const uint4 *__restrict__ x, const int32_t *__restrict__ ids,
+    const int32_t *__restrict__ rank, const int32_t *__restrict__ hist,
+    const int32_t *__restrict__ padded, const int32_t *__restrict__ counts,
+    int32_t *__restrict__ row_of, int32_t *__restrict__ tok_of, uint4 *__restrict__ xp, int T,
+    int nvec, int E, int k, int C, int token_blocks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x < token_blocks) {
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    int row = 0;
+    if (lane < k) {
+      const int e = ids[(int64_t)t * k + lane];
+      row = padded[e] + hist[(int64_t)e * C + t / kChunk] + rank[(int64_t)t * k + lane];
+      row_of[(int64_t)t * k + lane] = row;
+      tok_of[row] = t;
+    }
+    int rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xffffffffu, row, j);
+    const uint4 *src = x + (int64_t)t * nvec;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(src + v);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) xp[(int64_t)rows[j] * nvec + v] = val;
+    }
+  } else {
+    const int e = blockIdx.x - token_blocks;
+    const int r0 = padded[e] + counts[e], r1 = padded[e + 1];
+    const int64_t n = (int64_t)(r1 - r0) * nvec;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) xp[(int64_t)r0 * nvec + i] = zero;
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) tok_of[r] = -1;
+  }
+}
+
+// ------------------------------------------------------------------------- combine
+// One warp per token: y[t] = sum_j w[t][j] * o[row_of[t][j]], fp32 FMA in slot order,
+// one bf16 rounding. With unit weights it is the backward's dX gather-sum.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict__ o,
+                                                         const float *__restrict__ w,
+                                                         const int32_t *__restrict__ row_of,
+                                                         uint4 *__restrict__ y, int T, int nvec,
+                                                         int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  int row = 0;
+  float wt = 1.f;
+  if (lane < k) {
+    row = row_of[(int64_t)t * k + lane];
+    if (WEIGHTED) wt = w[(int64_t)t * k + lane];
+  }
+  int rows[kMaxK];
+  float wts[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    rows[j] = __shfl_sync(0xffffffffu, row, j);
+    wts[j] = __shfl_sync(0xffffffffu, wt, j);
+  }
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        float f[8];
+        unpack8(__ldg(o + (int64_t)rows[j] * nvec + v), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = WEIGHTED ? fmaf(wts[j], f[i], acc[i]) : acc[i] + f[i];
+      }
+    }
+    y[(int64_t)t * nvec + v] = pack8(acc);
+  }
+}
+
+// ------------------------------------------------------------------ backward scatter
+// G[row_of[t][j]] = bf16(w[t][j] * dY[t]) (one warp per token); the extra E blocks
+// zero each expert's padding rows of G so the GEMMs read zeros there.
+__global__ void __launch_bounds__(256) scale_scatter_kernel(
+    const uint4 *__restrict__ dy, const float *__restrict__ w, const int32_t *__restrict__ row_of,
+    const int32_t *__restrict__ padded, const int32_t *__restrict__ counts,
+    uint4 *__restrict__ g, int T, int nvec, int E, int k, int token_blocks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x < token_blocks) {
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    int row = 0;
+    float wt = 0.f;
+    if (lane < k) {
+      row = row_of[(int64_t)t * k + lane];
+      wt = w[(int64_t)t * k + lane];
+    }
+    int rows[kMaxK];
+    float wts[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, row, j);
+      wts[j] = __shfl_sync(0xffffffffu, wt, j);
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8];
+      unpack8(__ldg(dy + (int64_t)t * nvec + v), f);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          float s[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[i] = wts[j] * f[i];
+          g[(int64_t)rows[j] * nvec + v] = pack8(s);
+        }
+      }
+    }
+  } else {
+    const int e = blockIdx.x - token_blocks;
+    const int r0 = padded[e] + counts[e], r1 = padded[e + 1];
+    const int64_t n = (int64_t)(r1 - r0) * nvec;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) g[(int64_t)r0 * nvec + i] = zero;
+  }
+}
+
+// ------------------------------------------------------------------------ launchers
+static inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *rank,
+                         int32_t *hist, int T, int E, int k, bool with_count, cudaStream_t st) {
+  const int C = ceil_div(T, kChunk);
+  if (C == 0) return cudaSuccess;
+  if (with_count) {
+    launch_begin(st);
+    route_kernel<true><<<C, 256, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+    return note_launch("route_count", st);
+  }
+  launch_begin(st);
+  route_kernel<false><<<C, 256, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+  return note_launch("route", st);
+}
+
+cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,
+                         cudaStream_t st) {
+  const int C = ceil_div(T, kChunk);
+  if (C == 0) return cudaSuccess;
+  launch_begin(st);
+  count_kernel<<<C, 256, 0, st>>>(ids, rank, hist, T, E, k, C);
+  return note_launch("count", st);
+}
+
+cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
+                        int32_t *padded, int32_t *tile_expert, cudaStream_t st) {
+  const int C = ceil_div(T, kChunk);
+  launch_begin(st);
+  scan_kernel<<<1, 1024, 0, st>>>(hist, C, E, counts, offsets, padded, tile_expert);
+  return note_launch("scan", st);
+}
+
+cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t *padded,
+                        int32_t *tile_expert, cudaStream_t st) {
+  launch_begin(st);
+  plan_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, padded, tile_expert);
+  return note_launch("plan", st);
+}
+
+cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *rank,
+                           const int32_t *hist, const int32_t *padded, const int32_t *counts,
+                           int32_t *row_of, int32_t *tok_of, void *xp, int T, int d, int E, int k,
+                           cudaStream_t st) {
+  const int C = ceil_div(T, kChunk);
+  const int token_blocks = ceil_div(T, 8);
+  launch_begin(st);
+  scatter_kernel<<<token_blocks + E, 256, 0, st>>>(
+      (const uint4 *)x, ids, rank, hist, padded, counts, row_of, tok_of, (uint4 *)xp, T, d / 8,
+      E, k, C, token_blocks);
+  return note_launch("scatter", st);
+}
+
+cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of, void *y, int T,
+                           int d, int k, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  launch_begin(st);
+  gather_sum_kernel<true><<<ceil_div(T, 8), 256, 0, st>>>((const uint4 *)o, w, row_of,
+                                                          (uint4 *)y, T, d / 8, k);
+  return note_launch("combine", st);
+}
+
+cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, int T, int d,
+                              int k, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  launch_begin(st);
+  gather_sum_kernel<false><<<ceil_div(T, 8), 256, 0, st>>>((const uint4 *)dxp, nullptr, row_of,
+                                                           (uint4 *)dx, T, d / 8, k);
+  return note_launch("dx_gather", st);
+}
+
+cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *row_of,
+                                 const int32_t *padded, const int32_t *counts, void *g, int T,
+                                 int d, int E, int k, cudaStream_t st) {
+  const int token_blocks = ceil_div(T, 8);
+  launch_begin(st);
+  scale_scatter_kernel<<<token_blocks + E, 256, 0, st>>>((const uint4 *)dy, w, row_of, padded,
+                                                         counts, (uint4 *)g, T, d / 8, E, k,
+                                                         token_blocks);
+  return note_launch("g_scatter", st);
+}
+
+}  // namespace moe

@@ -278,7 +278,7 @@ def expert_members(ids: np.ndarray, w: np.ndarray, e: int) -> tuple[np.ndarray, 
 def dw_down_rows(e: int, rows: np.ndarray, x, dy, ids, w, w_gu, w_down) -> np.ndarray:
     """Rows i of dW_down[e] = sum over the expert's tokens of H[r, i] * G[r, :]."""
     toks, wts = expert_members(ids, w, e)
-    f = np.asarray(w_down).shape[1]
+    f = np.asarray(w_down[e]).shape[0]
     d = np.asarray(dy).shape[1]
     rows = np.asarray(rows)
     if len(toks) == 0:
@@ -295,7 +295,7 @@ def dw_down_rows(e: int, rows: np.ndarray, x, dy, ids, w, w_gu, w_down) -> np.nd
 def dw_gu_cols(e: int, cols: np.ndarray, x, dy, ids, w, w_gu, w_down) -> np.ndarray:
     """Columns c of dW_gu[e] = sum over the expert's tokens of Xp[r, :] * dGU[r, c]."""
     toks, wts = expert_members(ids, w, e)
-    f = np.asarray(w_down).shape[1]
+    f = np.asarray(w_down[e]).shape[0]
     d = np.asarray(x).shape[1]
     cols = np.asarray(cols)
     if len(toks) == 0:
