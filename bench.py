@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Throughput of the MoE expert block on GB300: forward + backward of one batch.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+One step is one pass of the whole block over one batch: route, dispatch,
+gate_up GEMM + SwiGLU, down GEMM, combine, then the backward (G scatter, dH GEMM +
+SwiGLU backward, dW_down, dXp GEMM, dW_gu, dX gather), through the C ABI on the
+gpt-oss-20b-like workload (T=4096 tokens, d=2880, E=32 experts, k=4, f=2880,
+seed 2; synthetic inputs). Rank 0 prints one JSON line.
+
+  value     tokens/s over all ranks, device-timed with CUDA events (L2 flushed
+            before every timed step, outside the timed events)
+  e2e       the same through the Python API with pinned host inputs copied in and
+            Y and dX copied out inside the timed region
+  roofline  the dominant kernel (largest share of step time): algorithmic work
+            per launch / its mean launch time from library-recorded CUDA events
+  cpu_baseline  the CPU oracle timed on the host cores on a bounded token sample
+  --impl reference  times the CPU oracle alone (rank 0), as the reference arm.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling, no data-path collective); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE layer tokens/s and grouped-GEMM TFLOPS (% of GB300 bf16 peak), 1 GPU"
+UNIT = "tokens/s"
+WORKLOAD = "gpt_oss_20b"
+L2_FLUSH_BYTES = 256 << 20       # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_SOURCES = ("moe_expert_layer_route_gb300/csrc/grouped_gemm.cu",
+                "moe_expert_layer_route_gb300/csrc/common.cuh")
+BW_SOURCES = ("moe_expert_layer_route_gb300/csrc/route_dispatch.cu",
+              "moe_expert_layer_route_gb300/csrc/common.cuh")
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of the ranks' values (all ranks get it)."""
+    if world == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- helpers
+def peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_work(wl: workloads.Workload) -> dict:
+    """Algorithmic work of one launch of each kernel: ('flop'|'byte', amount)."""
+    T, d, E, k, f, A = wl.T, wl.d, wl.E, wl.k, wl.f, wl.A
+    C = (T + 31) // 32
+    return {
+        "gemm_gate_up_swiglu": ("flop", 4 * A * d * f),
+        "gemm_down": ("flop", 2 * A * d * f),
+        "gemm_dgrad_h_swiglu_bwd": ("flop", 2 * A * d * f),
+        "gemm_wgrad_down": ("flop", 2 * A * d * f),
+        "gemm_dgrad_x": ("flop", 4 * A * d * f),
+        "gemm_wgrad_gu": ("flop", 4 * A * d * f),
+        # bandwidth kernels: bytes the stage must move at least once
+        "route_count": ("byte", T * E * 4 + A * 12 + E * C * 4),
+        "scan": ("byte", 2 * E * C * 4),
+        "scatter": ("byte", T * d * 2 + A * d * 2 + A * 16),
+        "combine": ("byte", A * d * 2 + A * 8 + T * d * 2),
+        "g_scatter": ("byte", T * d * 2 + A * d * 2 + A * 8),
+        "dx_gather": ("byte", A * d * 2 + A * 4 + T * d * 2),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict | None:
+        if self.proc is None or self.path is None:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = max(mx, float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- CPU oracle
+def oracle_step(oracle, inp_np: dict, n_tok: int, k: int) -> float:
+    """Forward + backward of the oracle on the first n_tok tokens; returns seconds."""
+    t0 = time.perf_counter()
+    ref = oracle.forward(inp_np["x"][:n_tok], inp_np["logits"][:n_tok], inp_np["w_gu"],
+                         inp_np["w_down"], k)
+    oracle.backward(inp_np["dy"][:n_tok], ref, inp_np["w_gu"], inp_np["w_down"])
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(inp: workloads.Inputs) -> dict:
+    return {"x": inp.x.float().numpy(), "logits": inp.logits.numpy(),
+            "w_gu": inp.w_gu.float().numpy(), "w_down": inp.w_down.float().numpy(),
+            "dy": inp.dy.float().numpy()}
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except ImportError:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, inp, seconds: float) -> dict:
+    """The oracle as it stands on a bounded token sample sized to about `seconds`."""
+    import oracle
+    inp_np = oracle_inputs(inp)
+    n = 16
+    t = oracle_step(oracle, inp_np, n, wl.k)
+    while t < seconds / 4 and n < wl.T:
+        n = min(wl.T, n * 4)
+        t = oracle_step(oracle, inp_np, n, wl.k)
+    return {"value": n / t, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of the {wl.name} workload, forward+backward "
+                      f"in fp64 numpy, {t:.1f} s"}
+
+
+# ---------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank) -> dict | None:
+    import moe_expert_layer_route_gb300 as moe
+    from moe_expert_layer_route_gb300 import _build
+    if rank == 0 or not _build.up_to_date():
+        if world == 1 or local_rank == 0:
+            _build.build()
+    barrier(world)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl, with_dy=True)
+    x, logits = inp.x.to(dev), inp.logits.to(dev)
+    w_gu, w_down, dy = inp.w_gu.to(dev), inp.w_down.to(dev), inp.dy.to(dev)
+    s = moe.shape(wl.T, wl.d, wl.E, wl.k, wl.f)
+    ws = moe.new_workspace(s, True, dev)
+    scratch = moe.new_scratch(s, dev)
+    y = torch.empty_like(x)
+    grads = (torch.empty_like(x), torch.empty_like(w_gu), torch.empty_like(w_down))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        moe.forward(x, logits, w_gu, w_down, wl.k, training=True, ws=ws, y=y)
+        moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    moe.check_device_status(ws)
+    moe.check_device_status(scratch)
+
+    # ---- device-timed region
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
+    launches0 = moe.launch_count()
+    moe.profile_start(capacity=K * 16)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        for i in range(K):
+            flush.zero_()
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    records = moe.profile_stop(capacity=K * 16)
+    launches = moe.launch_count() - launches0
+    moe.check_device_status(ws)
+    moe.check_device_status(scratch)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    tokens_all = sum_over_ranks(wl.T, world, dev)
+
+    # ---- per-kernel times and the roofline of the dominant kernel
+    per = {}
+    for name, t in records:
+        per.setdefault(name, []).append(t)
+    work = kernel_work(wl)
+    pk, peak_src = peaks()
+    stages = {}
+    for name, ts in per.items():
+        kind, amount = work.get(name, ("byte", 0))
+        mean = statistics.mean(ts)
+        entry = {"launches_per_step": len(ts) / K, "ms": mean,
+                 "share": sum(ts) / max(sum(sum(v) for v in per.values()), 1e-9)}
+        if amount:
+            if kind == "flop":
+                entry.update(achieved=amount / (mean * 1e-3) / 1e12, unit="TFLOP/s",
+                             frac=amount / (mean * 1e-3) / 1e12 / pk["bf16_tflops_sustained"])
+            else:
+                entry.update(achieved=amount / (mean * 1e-3) / 1e9, unit="GB/s",
+                             frac=amount / (mean * 1e-3) / 1e9 / pk["hbm_gbs"])
+        stages[name] = entry
+    dom = max(per, key=lambda n: sum(per[n]))
+    dkind, damount = work[dom]
+    dmean = statistics.mean(per[dom])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as fh:
+            tr = json.load(fh).get(dom)
+        srcs = GEMM_SOURCES if dom.startswith("gemm") else BW_SOURCES
+        if tr and tr.get("source_hash") == source_hash(srcs) and tr.get("workload") == wl.name:
+            traffic = tr.get("bytes_per_launch")
+    if dkind == "flop":
+        ach = damount / (dmean * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"],
+                "traffic": traffic, "kernel": dom,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+    else:
+        ach = damount / (dmean * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "traffic": traffic, "kernel": dom,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    gemm_names = [n for n in per if n.startswith("gemm")]
+    gemm_flop = sum(work[n][1] * len(per[n]) for n in gemm_names) / K
+    gemm_ms = sum(sum(per[n]) for n in gemm_names) / K
+    gemm_tflops = gemm_flop / (gemm_ms * 1e-3) / 1e12
+
+    # ---- end to end through the Python API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = inp.x.pin_memory()
+        hl = inp.logits.pin_memory()
+        hdy = inp.dy.pin_memory()
+        hy = torch.empty_like(hx).pin_memory()
+        hdx = torch.empty_like(hx).pin_memory()
+        ke = max(3, min(K, 50))
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            logits.copy_(hl, non_blocking=True)
+            dy.copy_(hdy, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+            hdx.copy_(grads[0], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(ke):
+            e2e_step()
+        ev1.record()
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) * 1e3 / ke
+        e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
+        h2d = hx.numel() * 2 + hl.numel() * 4 + hdy.numel() * 2
+        d2h = hy.numel() * 2 + hdx.numel() * 2
+        e2e = {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return None
+    out = {
+        "metric": METRIC, "value": tokens_all / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
+                   "f": wl.f, "seed": wl.seed, "passes": "forward+backward",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed (256 MB write) before each timed step, outside its events; "
+                         "weights alone are 2.1 GB"},
+        "gemm_tflops": gemm_tflops,
+        "gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16_tflops_sustained"],
+        "gemm_flop_per_step": gemm_flop,
+        "roofline": roof,
+        "stages": stages,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    return out
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank, world) -> dict | None:
+    """The CPU oracle as the reference arm: each step a bounded token sample."""
+    if rank != 0:
+        return None
+    import oracle
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl, with_dy=True)
+    inp_np = oracle_inputs(inp)
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    n = 4
+    t = oracle_step(oracle, inp_np, n, wl.k)
+    while t < budget / 2 and n * 2 <= wl.T:
+        n *= 2
+        t = oracle_step(oracle, inp_np, n, wl.k)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_step(oracle, inp_np, n, wl.k)
+    times = [oracle_step(oracle, inp_np, n, wl.k) for _ in range(args.steps)]
+    sec = statistics.mean(times)
+    value = n / sec
+    cores = cpu_threads()
+    sample = (f"first {n} of {wl.T} tokens of the {wl.name} workload per step, "
+              f"forward+backward in fp64 numpy")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
+                   "f": wl.f, "seed": wl.seed, "passes": "forward+backward"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=150.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        dist_init(world, "nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

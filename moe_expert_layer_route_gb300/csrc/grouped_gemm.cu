@@ -567,7 +567,7 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
 }
 
 cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
-                       int *status, cudaStream_t st) {
+                       int *status, const char *name, cudaStream_t st) {
   CUtensorMap tA, tB;
   cudaError_t e = map2d(&tA, x, M, p.R, 64, 64);
   if (e != cudaSuccess) return e;
@@ -579,7 +579,7 @@ cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw
   a.M_out = M;
   a.N_out = N;
   a.out = dw;
-  return launch_kind<WGRAD>(tA, tB, a, (int64_t)p.E * a.m_tiles * a.n_tiles, "gemm_wgrad", st);
+  return launch_kind<WGRAD>(tA, tB, a, (int64_t)p.E * a.m_tiles * a.n_tiles, name, st);
 }
 
 }  // namespace moe

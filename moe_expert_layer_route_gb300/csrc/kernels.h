@@ -70,7 +70,7 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
 // dW[e] (M x N, bf16, row-major, experts contiguous) = X_e^T Y_e over the padded
 // segment rows of expert e; X is R x M, Y is R x N.
 cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
-                       int *status, cudaStream_t st);
+                       int *status, const char *name, cudaStream_t st);
 
 // Driver entry point for cuTensorMapEncodeTiled (resolved once).
 cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,

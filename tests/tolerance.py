@@ -1,9 +1,15 @@
 """Error metrics used by the parity tests.
 
 The block's outputs and gradients (Y, dX, dW_gu, dW_down, and the stage outputs
-H and O) must satisfy, per tensor, ||gpu - ref||_F / ||ref||_F <= 2e-2 and
-max|gpu - ref| / rms(ref) <= 5e-2, rms(ref) = ||ref||_F / sqrt(n): the bf16-input
-bound for the block's floating-point results.
+H, GU and O) must satisfy, per tensor:
+  normwise   ||gpu - ref||_F / ||ref||_F <= 2e-2
+  elementwise max_i |gpu_i - ref_i| / max(|ref_i|, rms(ref)) <= 5e-2,
+              rms(ref) = ||ref||_F / sqrt(n).
+Each element's error is normalised by its own magnitude, floored at the tensor's
+rms: a single bf16 rounding (relative 2^-9) can never break the element bound, a
+wrong term or index does. Normalising every element by rms alone fails on
+heavy-tailed tensors (a skewed expert load makes dW mostly zeros plus a few large
+experts) from output rounding alone.
 """
 import numpy as np
 
@@ -23,12 +29,13 @@ def errors(got, ref) -> tuple[float, float]:
     if nref == 0.0:
         return float(np.linalg.norm(diff)), float(np.abs(diff).max(initial=0.0))
     rms = nref / np.sqrt(ref.size)
-    return float(np.linalg.norm(diff) / nref), float(np.abs(diff).max(initial=0.0) / rms)
+    scale = np.maximum(np.abs(ref), rms)
+    return float(np.linalg.norm(diff) / nref), float((np.abs(diff) / scale).max(initial=0.0))
 
 
 def assert_close(got, ref, name: str = "", norm_rel: float = NORM_REL,
                  max_rel_rms: float = MAX_REL_RMS) -> tuple[float, float]:
     nr, mr = errors(got, ref)
     assert nr <= norm_rel and mr <= max_rel_rms, (
-        f"{name}: normwise rel {nr:.3e} (limit {norm_rel}), max/rms {mr:.3e} (limit {max_rel_rms})")
+        f"{name}: normwise rel {nr:.3e} (limit {norm_rel}), elementwise {mr:.3e} (limit {max_rel_rms})")
     return nr, mr
