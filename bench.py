@@ -224,6 +224,19 @@ def cpu_baseline(wl, inp, seconds: float) -> dict:
 
 
 # ---------------------------------------------------------------------- our arm
+def workload_of(args) -> workloads.Workload:
+    wl = workloads.WORKLOADS[args.workload]
+    over = {}
+    if args.tokens is not None:
+        over["T"] = args.tokens
+    if args.experts is not None:
+        over["E"] = args.experts
+    if over:
+        desc = wl.description + " with " + ", ".join(f"{k}={v}" for k, v in over.items())
+        wl = wl.scaled(description=desc, **over)
+    return wl
+
+
 def run_ours(args, rank, world, local_rank) -> dict | None:
     import moe_expert_layer_route_gb300 as moe
     from moe_expert_layer_route_gb300 import _build
@@ -233,7 +246,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     barrier(world)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = workloads.WORKLOADS[args.workload]
+    wl = workload_of(args)
     inp = workloads.make_inputs(wl, with_dy=True)
     x, logits = inp.x.to(dev), inp.logits.to(dev)
     w_gu, w_down, dy = inp.w_gu.to(dev), inp.w_down.to(dev), inp.dy.to(dev)
@@ -309,7 +322,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         with open(tpath) as fh:
             tr = json.load(fh).get(dom)
         srcs = GEMM_SOURCES if dom.startswith("gemm") else BW_SOURCES
-        if tr and tr.get("source_hash") == source_hash(srcs) and tr.get("workload") == wl.name:
+        if tr and tr.get("source_hash") == source_hash(srcs) and \
+                tr.get("workload") == wl.description:
             traffic = tr.get("bytes_per_launch")
     if dkind == "flop":
         ach = damount / (dmean * 1e-3) / 1e12
@@ -395,7 +409,7 @@ def run_reference(args, rank, world) -> dict | None:
     if rank != 0:
         return None
     import oracle
-    wl = workloads.WORKLOADS[args.workload]
+    wl = workload_of(args)
     inp = workloads.make_inputs(wl, with_dy=True)
     inp_np = oracle_inputs(inp)
     budget = args.reference_seconds / max(1, args.steps + args.warmup)
@@ -436,6 +450,10 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (profiling a smaller case; not a headline line)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (profiling a smaller case; not a headline line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -101,7 +101,7 @@ typedef struct {
   int32_t *offsets; /* E + 1   compact segment starts (exclusive prefix of counts) */
   int32_t *padded_offsets; /* E + 1   segment starts P_e in the padded row space */
   int32_t *row_of;  /* T x k   padded row of assignment (t, j) */
-  int32_t *tok_of;  /* R       token of each padded row, -1 on padding rows */
+  int32_t *tok_of;  /* R       token of each padded row, -1 on padding rows and past P_E */
   moe_bf16 *xp;     /* R x d   dispatched token rows */
   moe_bf16 *gu;     /* R x 2f  gate|up pre-activations (training only) */
   moe_bf16 *h;      /* R x f   SwiGLU activations */
@@ -127,7 +127,9 @@ moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w, m
  *   x [T x d] bf16 in; ids [T x k] int32 in (each row k distinct experts in [0, E));
  *   xp [R x d] bf16 out (padding rows zeroed); counts [E], offsets [E+1] int32 out
  *   (compact, offsets[E] = T*k); padded_offsets [E+1] int32 out (P_e);
- *   row_of [T x k] int32 out (padded row of (t, j)); tok_of [R] int32 out (-1 on padding).
+ *   row_of [T x k] int32 out (padded row of (t, j)); tok_of [R] int32 out (-1 on padding
+ *   rows and on the rows at and past padded_offsets[E], which belong to no expert; xp is
+ *   not written there).
  * Uses ws (at least moe_workspace_size(s, 0) bytes) for the block histograms. */
 moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xp,
                         int32_t *counts, int32_t *offsets, int32_t *padded_offsets,

@@ -29,7 +29,7 @@ cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t 
 cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *rank,
                            const int32_t *hist, const int32_t *padded, const int32_t *counts,
                            int32_t *row_of, int32_t *tok_of, void *xp, int T, int d, int E, int k,
-                           cudaStream_t st);
+                           int R, cudaStream_t st);
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of, void *y, int T,
                            int d, int k, cudaStream_t st);
 cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, int T, int d,

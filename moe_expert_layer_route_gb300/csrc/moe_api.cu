@@ -241,7 +241,7 @@ moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_
   MOE_CUDA(launch_scan(hist, T, E, counts, offsets, padded_offsets, at<int32_t>(ws, L.tile_expert),
                        st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded_offsets, counts, row_of, tok_of, xp, T, d, E,
-                          k, st));
+                          k, (int)padded_rows(s), st));
   return MOE_OK;
 }
 
@@ -299,7 +299,8 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_route(logits, ids, w, rank, hist, T, E, k, true, st));
   MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, st));
-  MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k, st));
+  MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
+                          (int)padded_rows(s), st));
   const GemmPlan p{padded, tiles, E, padded_rows(s)};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));

@@ -221,12 +221,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 // slot j (segment start + chunk base + local rank), then the warp copies x[t] to each
 // of its k rows in 16-byte vectors (read once, written k times).
 // Blocks [token_blocks, token_blocks + E): block e zeroes expert e's padding rows.
+// The last block marks the rows past the last segment (up to R) with tok_of = -1.
 __global__ void __launch_bounds__(256) scatter_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ ids,
     const int32_t *__restrict__ rank, const int32_t *__restrict__ hist,
     const int32_t *__restrict__ padded, const int32_t *__restrict__ counts,
     int32_t *__restrict__ row_of, int32_t *__restrict__ tok_of, uint4 *__restrict__ xp, int T,
-    int nvec, int E, int k, int C, int token_blocks) {
+    int nvec, int E, int k, int C, int token_blocks, int R) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x < token_blocks) {
     const int t = blockIdx.x * 8 + warp;
@@ -248,13 +249,16 @@ __global__ void __launch_bounds__(256) scatter_kernel(
       for (int j = 0; j < kMaxK; ++j)
         if (j < k) xp[(int64_t)rows[j] * nvec + v] = val;
     }
-  } else {
+  } else if ((int)blockIdx.x < token_blocks + E) {
     const int e = blockIdx.x - token_blocks;
     const int r0 = padded[e] + counts[e], r1 = padded[e + 1];
     const int64_t n = (int64_t)(r1 - r0) * nvec;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) xp[(int64_t)r0 * nvec + i] = zero;
     for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) tok_of[r] = -1;
+  } else {
+    // rows past the last segment belong to no expert
+    for (int r = padded[E] + threadIdx.x; r < R; r += blockDim.x) tok_of[r] = -1;
   }
 }
 
@@ -390,13 +394,13 @@ cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t 
 cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *rank,
                            const int32_t *hist, const int32_t *padded, const int32_t *counts,
                            int32_t *row_of, int32_t *tok_of, void *xp, int T, int d, int E, int k,
-                           cudaStream_t st) {
+                           int R, cudaStream_t st) {
   const int C = ceil_div(T, kChunk);
   const int token_blocks = ceil_div(T, 8);
   launch_begin(st);
-  scatter_kernel<<<token_blocks + E, 256, 0, st>>>(
+  scatter_kernel<<<token_blocks + E + 1, 256, 0, st>>>(
       (const uint4 *)x, ids, rank, hist, padded, counts, row_of, tok_of, (uint4 *)xp, T, d / 8,
-      E, k, C, token_blocks);
+      E, k, C, token_blocks, R);
   return note_launch("scatter", st);
 }
 

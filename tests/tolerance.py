@@ -7,10 +7,16 @@ H, GU and O) must satisfy, per tensor:
               rms(ref) = ||ref||_F / sqrt(n).
 Each element's error is normalised by its own magnitude, floored at the tensor's
 rms: a single bf16 rounding (relative 2^-9) can never break the element bound, a
-wrong term or index does. Normalising every element by rms alone fails on
-heavy-tailed tensors (a skewed expert load makes dW mostly zeros plus a few large
-experts) from output rounding alone.
+wrong term or index does. The expert weight gradients dW_gu and dW_down are E
+independent matrices whose scales follow each expert's load (a skewed load gives
+one expert every token and leaves others empty), so they are checked expert by
+expert (assert_close_experts): each non-empty expert's slice against the bound,
+each empty expert's slice exactly zero.
+
+Setting MOE_PARITY_LOG=<file> appends every checked error to that file.
 """
+import os
+
 import numpy as np
 
 NORM_REL = 2e-2
@@ -36,6 +42,33 @@ def errors(got, ref) -> tuple[float, float]:
 def assert_close(got, ref, name: str = "", norm_rel: float = NORM_REL,
                  max_rel_rms: float = MAX_REL_RMS) -> tuple[float, float]:
     nr, mr = errors(got, ref)
+    log = os.environ.get("MOE_PARITY_LOG")
+    if log:
+        with open(log, "a") as fh:
+            fh.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]}\t{name}\t"
+                     f"normwise={nr:.3e}\telementwise={mr:.3e}\n")
     assert nr <= norm_rel and mr <= max_rel_rms, (
         f"{name}: normwise rel {nr:.3e} (limit {norm_rel}), elementwise {mr:.3e} (limit {max_rel_rms})")
     return nr, mr
+
+
+def assert_close_experts(got, ref, name: str = "") -> None:
+    """Per-expert check of a [E, ...] weight gradient (see the module docstring)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    worst = (0.0, 0.0)
+    for e in range(ref.shape[0]):
+        if not ref[e].any():
+            assert not got[e].any(), f"{name}[{e}]: an expert without tokens must get zeros"
+            continue
+        nr, mr = errors(got[e], ref[e])
+        worst = (max(worst[0], nr), max(worst[1], mr))
+        assert nr <= NORM_REL and mr <= MAX_REL_RMS, (
+            f"{name}[{e}]: normwise rel {nr:.3e} (limit {NORM_REL}), elementwise {mr:.3e} "
+            f"(limit {MAX_REL_RMS})")
+    log = os.environ.get("MOE_PARITY_LOG")
+    if log:
+        with open(log, "a") as fh:
+            fh.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]}\t{name} "
+                     f"(worst expert)\tnormwise={worst[0]:.3e}\telementwise={worst[1]:.3e}\n")
