@@ -187,6 +187,27 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
                         moe_bf16 *dw_gu, moe_bf16 *dw_down, void *scratch, size_t scratch_bytes,
                         moe_stream stream);
 
+/* Dispatch without a workspace, for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call: it exists for callers that have no
+ * way to obtain device memory for a workspace (code running under a runtime that
+ * owns every allocation, or that must not call cudaMalloc at that point). It
+ * computes exactly what moe_dispatch computes, with the same arguments minus ws and
+ * ws_bytes, and allocates nothing: its scratch (local ranks, chunk histograms, the
+ * tile-to-expert table) is a file-scope __device__ array of 4 MiB (2^20 int32) that
+ * every GPU loading the library holds until exit.
+ *   Limit: round64(T*k) + round64(E*ceil(T/32)) + round64(R/128) <= 2^20 int32,
+ *   round64(n) = n rounded up to a multiple of 64 and R = moe_padded_rows(s)
+ *   (T = 65536 with E = 32 and k = 4 fits). Larger shapes return MOE_ERR_WORKSPACE.
+ *   The first call on a device looks up the array's device address (set-up, once
+ *   per device, with that device current); make that first call before any stream
+ *   capture. Every call shares the one array and it keeps the last call's contents:
+ *   each call writes every entry it reads, so nothing needs clearing, but calls that
+ *   overlap on the GPU (other streams or host threads) race and must be ordered by
+ *   the caller. */
+moe_status moe_dispatch_noalloc(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xp,
+                                int32_t *counts, int32_t *offsets, int32_t *padded_offsets,
+                                int32_t *row_of, int32_t *tok_of, moe_stream stream);
+
 /* Device-side status of a workspace or scratch: synchronises `stream`, reads the
  * status word that the kernels set when a pipeline wait runs past its time limit,
  * and clears it. Returns MOE_OK or MOE_ERR_TIMEOUT. */

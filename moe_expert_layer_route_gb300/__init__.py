@@ -55,6 +55,8 @@ _SIG = {
     "moe_expert_ffn": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                       _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_combine": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                            _c_vp, _c_vp, _c_vp]),
     "moe_forward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_int,
                                    _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
@@ -221,6 +223,25 @@ def dispatch(s: MoEShape, x: torch.Tensor, ids: torch.Tensor, ws: torch.Tensor |
     return out
 
 
+def dispatch_noalloc(s: MoEShape, x: torch.Tensor, ids: torch.Tensor) -> dict:
+    """moe_dispatch_noalloc: moe_dispatch without a workspace (fixed 4 MiB device scratch)."""
+    _want(x, torch.bfloat16, "x")
+    _want(ids, torch.int32, "ids")
+    dev = x.device
+    R = padded_rows(s)
+    out = {"xp": torch.empty((R, s.d), dtype=torch.bfloat16, device=dev),
+           "counts": torch.empty((s.E,), dtype=torch.int32, device=dev),
+           "offsets": torch.empty((s.E + 1,), dtype=torch.int32, device=dev),
+           "padded_offsets": torch.empty((s.E + 1,), dtype=torch.int32, device=dev),
+           "row_of": torch.empty((s.T, s.k), dtype=torch.int32, device=dev),
+           "tok_of": torch.empty((R,), dtype=torch.int32, device=dev)}
+    _check(lib().moe_dispatch_noalloc(s, _p(x), _p(ids), _p(out["xp"]), _p(out["counts"]),
+                                      _p(out["offsets"]), _p(out["padded_offsets"]),
+                                      _p(out["row_of"]), _p(out["tok_of"]), _stream()),
+           "moe_dispatch_noalloc")
+    return out
+
+
 def expert_ffn(s: MoEShape, xp: torch.Tensor, counts: torch.Tensor, w_gu: torch.Tensor,
                w_down: torch.Tensor, save_gu: bool = False, ws: torch.Tensor | None = None
                ) -> tuple[torch.Tensor, torch.Tensor | None, torch.Tensor]:
@@ -311,5 +332,5 @@ def launch_count() -> int:
 
 __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
-           "dispatch", "expert_ffn", "combine", "forward", "backward", "check_device_status",
+           "dispatch", "dispatch_noalloc", "expert_ffn", "combine", "forward", "backward", "check_device_status",
            "profile_start", "profile_stop", "launch_count", "LIB_PATH"]
