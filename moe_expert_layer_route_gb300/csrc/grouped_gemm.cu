@@ -30,9 +30,20 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box (MN-major tiles are built of these)
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+// epilogue staging: per epilogue warp two 32-row x 32-column bf16 buffers (2 KB each,
+// 64-byte swizzled like the TMA store expects)
+constexpr int kStageOutBytes = 32 * 32 * 2;
+constexpr int kEpiSmem = kEpiWarps * 2 * kStageOutBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiSmem + 1024;
+#ifndef MOE_GEMM_PREFETCH
+#define MOE_GEMM_PREFETCH 0
+#endif
+// k-blocks of weight tiles prefetched into L2 ahead of the smem ring (0 = off; on
+// GB300 every distance tried, 4 and 8, made the ragged-M GEMMs slower)
+constexpr int kPrefetch = MOE_GEMM_PREFETCH;
 
 enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
 
@@ -46,10 +57,7 @@ struct Args {
   int M_out;    // WGRAD: rows of dW[e]
   int N_out;    // valid output columns
   int f;        // SwiGLU width (GATE_UP, DGRAD_H)
-  void *out;
-  int64_t ld_out;
-  void *out2;   // GATE_UP: GU saved (or null)
-  int64_t ld_out2;
+  void *out2;       // GATE_UP: GU saved (null when not training)
   const void *aux;  // DGRAD_H: GU
   int64_t ld_aux;
   int *status;
@@ -121,120 +129,220 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap *tmA, const CUtens
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
-__device__ __forceinline__ void store8(void *base, int64_t idx, const float (&v)[8]) {
-  *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(base) + idx) = pack8(v);
+// One epilogue warp's two staging buffers, used as a ring: each staged output chunk
+// (32 rows x 32 columns) takes the next buffer once the bulk store that last read it
+// is done, then leaves smem by one TMA store.
+struct Stager {
+  uint8_t *base;
+  int n;
+  __device__ __forceinline__ uint8_t *next(int lane) {
+    uint8_t *b = base + (n & 1) * kStageOutBytes;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return b;
+  }
+  // both buffers at once (two outputs from one pass over the accumulator)
+  __device__ __forceinline__ void both(int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+  }
+  // lane's row (64 bytes), 16-byte chunk j (columns 8j..8j+7), 64-byte swizzle: the
+  // chunk index is XORed with bits 7..8 of the offset, i.e. (row / 2) % 4
+  static __device__ __forceinline__ void put(uint8_t *b, int lane, int j, const float (&v)[8]) {
+    *reinterpret_cast<uint4 *>(b + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = pack8(v);
+  }
+  __device__ __forceinline__ void publish() {
+    fence_proxy_async_shared();
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ void put32(uint8_t *b, int lane, const float (&x)[32]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = x[8 * v + i];
+    Stager::put(b, lane, v, o);
+  }
 }
 
-__device__ __forceinline__ void load8(const void *base, int64_t idx, float (&v)[8]) {
-  unpack8(*reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + idx), v);
-}
-
+// Epilogue of one tile for one warp: TMEM lanes of quarter q (rows m0+32q ..), the
+// accumulator columns of half ch of the tile.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Args &a, const Tile &t, uint32_t taddr,
-                                              int row_in_tile) {
+                                              int q, int ch, int lane, Stager &st,
+                                              const CUtensorMap *tmO, const CUtensorMap *tmO2) {
+  const int row0 = t.m0 + 32 * q;  // first row of this warp's 32-row slab
   if (KIND == GATE_UP) {
-    const int64_t row = t.m0 + row_in_tile;
+    // accumulator columns [0,128) gate, [128,256) up; this warp: h columns ch*64 ..+63
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+    for (int c32 = ch * 64; c32 < ch * 64 + 64; c32 += 32) {
+      const int col = t.n0 + c32;
+      if (col >= a.f) break;
       float g[32], u[32];
-      tmem_ld32x2(taddr + c0, taddr + BN / 2 + c0, g, u);
-      const int col = t.n0 + c0;
+      tmem_ld32x2(taddr + c32, taddr + BN / 2 + c32, g, u);
+      uint8_t *b = st.next(lane);
+      {
+        float h[32];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int c = col + 8 * v;
-        if (c < a.f) {
-          float h[8], gg[8], uu[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            gg[i] = g[8 * v + i];
-            uu[i] = u[8 * v + i];
-            h[i] = silu(gg[i]) * uu[i];
-          }
-          store8(a.out, row * a.ld_out + c, h);
-          if (a.out2) {
-            store8(a.out2, row * a.ld_out2 + c, gg);
-            store8(a.out2, row * a.ld_out2 + a.f + c, uu);
-          }
+        for (int i = 0; i < 32; ++i) h[i] = silu(g[i]) * u[i];
+        put32(b, lane, h);
+      }
+      st.publish();
+      if (lane == 0) {
+        tma_store_2d(tmO, b, col, row0);
+        bulk_commit();
+      }
+      ++st.n;
+      if (a.out2) {
+        uint8_t *bg = st.next(lane);
+        put32(bg, lane, g);
+        st.publish();
+        if (lane == 0) {
+          tma_store_3d(tmO2, bg, col, 0, row0);
+          bulk_commit();
         }
+        ++st.n;
+        uint8_t *bu = st.next(lane);
+        put32(bu, lane, u);
+        st.publish();
+        if (lane == 0) {
+          tma_store_3d(tmO2, bu, col, 1, row0);
+          bulk_commit();
+        }
+        ++st.n;
       }
     }
   } else if (KIND == DOWN || KIND == DGRAD_X) {
-    const int64_t row = t.m0 + row_in_tile;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float acc[32];
-      tmem_ld32(taddr + c0, acc);
-      const int col = t.n0 + c0;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int c = col + 8 * v;
-        if (c < a.N_out) {
-          float o[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[i] = acc[8 * v + i];
-          store8(a.out, row * a.ld_out + c, o);
-        }
+    for (int c32 = ch * 128; c32 < ch * 128 + 128; c32 += 32) {
+      const int col = t.n0 + c32;
+      if (col >= a.N_out) break;
+      float x[32];
+      tmem_ld32(taddr + c32, x);
+      uint8_t *b = st.next(lane);
+      put32(b, lane, x);
+      st.publish();
+      if (lane == 0) {
+        tma_store_2d(tmO, b, col, row0);
+        bulk_commit();
       }
+      ++st.n;
     }
   } else if (KIND == DGRAD_H) {
-    const int64_t row = t.m0 + row_in_tile;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float dh[32];
-      tmem_ld32(taddr + c0, dh);
-      const int col = t.n0 + c0;
+    // dH -> (dgate, dup) with the saved gate/up pre-activations of this row; the
+    // gate/up values of the next 32 columns are loaded while these are computed.
+    const int64_t row = row0 + lane;
+    const uint16_t *gu = reinterpret_cast<const uint16_t *>(a.aux) + row * a.ld_aux;
+    uint4 cg[4], cu[4], ng[4], nu[4];
+    auto load = [&](int c, uint4 (&g4)[4], uint4 (&u4)[4]) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const int c = col + 8 * v;
-        if (c < a.f) {
-          float g[8], u[8], dg[8], du[8];
-          load8(a.aux, row * a.ld_aux + c, g);
-          load8(a.aux, row * a.ld_aux + a.f + c, u);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float s = 1.f / (1.f + __expf(-g[i]));
-            const float x = dh[8 * v + i];
-            dg[i] = x * u[i] * s * (1.f + g[i] * (1.f - s));
-            du[i] = x * g[i] * s;
-          }
-          store8(a.out, row * a.ld_out + c, dg);
-          store8(a.out, row * a.ld_out + a.f + c, du);
+        if (c + 8 * v < a.f) {
+          g4[v] = ldg_nc(gu + c + 8 * v);
+          u4[v] = ldg_nc(gu + a.f + c + 8 * v);
+        } else {
+          g4[v] = make_uint4(0, 0, 0, 0);
+          u4[v] = make_uint4(0, 0, 0, 0);
         }
+      }
+    };
+    const int c_begin = ch * 128, c_end = ch * 128 + 128;
+    load(t.n0 + c_begin, cg, cu);
+#pragma unroll 1
+    for (int c32 = c_begin; c32 < c_end; c32 += 32) {
+      const int col = t.n0 + c32;
+      if (col >= a.f) break;
+      if (c32 + 32 < c_end) load(col + 32, ng, nu);
+      float dh[32];
+      tmem_ld32(taddr + c32, dh);
+      st.both(lane);
+      uint8_t *bg = st.base, *bu = st.base + kStageOutBytes;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float g[8], u[8], dg[8], du[8];
+        unpack8(cg[v], g);
+        unpack8(cu[v], u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float s = 1.f / (1.f + __expf(-g[i]));
+          const float x = dh[8 * v + i];
+          dg[i] = x * u[i] * s * (1.f + g[i] * (1.f - s));
+          du[i] = x * g[i] * s;
+        }
+        Stager::put(bg, lane, v, dg);
+        Stager::put(bu, lane, v, du);
+      }
+      st.publish();
+      if (lane == 0) {
+        tma_store_3d(tmO, bg, col, 0, row0);
+        tma_store_3d(tmO, bu, col, 1, row0);
+        bulk_commit();
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        cg[v] = ng[v];
+        cu[v] = nu[v];
       }
     }
   } else {  // WGRAD
-    const int m = t.m0 + row_in_tile;
-    const int64_t base = (int64_t)t.e * a.M_out * a.N_out + (int64_t)m * a.N_out;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float acc[32];
+    for (int c32 = ch * 128; c32 < ch * 128 + 128; c32 += 32) {
+      const int col = t.n0 + c32;
+      if (col >= a.N_out || row0 >= a.M_out) break;
+      float x[32];
       if (t.kt > 0) {
-        tmem_ld32(taddr + c0, acc);
+        tmem_ld32(taddr + c32, x);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 32; ++i) x[i] = 0.f;
       }
-      const int col = t.n0 + c0;
-      if (m < a.M_out) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int c = col + 8 * v;
-          if (c < a.N_out) {
-            float o[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = acc[8 * v + i];
-            store8(a.out, base + c, o);
-          }
-        }
+      uint8_t *b = st.next(lane);
+      put32(b, lane, x);
+      st.publish();
+      if (lane == 0) {
+        tma_store_3d(tmO, b, col, row0, t.e);
+        bulk_commit();
       }
+      ++st.n;
     }
+  }
+}
+
+// Before a DGRAD_H tile's accumulator is ready: pull this thread's row of the saved
+// gate/up values for the tile's columns into L2, so the epilogue's loads hit L2.
+__device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, int row, int ch) {
+  const char *base = reinterpret_cast<const char *>(a.aux) + (int64_t)row * a.ld_aux * 2;
+  const int c_end = min(t.n0 + ch * 128 + 128, a.f);
+#pragma unroll 1
+  for (int c = t.n0 + ch * 128; c < c_end; c += 64) {  // 64 bf16 = one 128-byte line
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 2 * (int64_t)c));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 2 * ((int64_t)a.f + c)));
+  }
+}
+
+// L2 prefetch of the weight (B) tiles of one k-block of a ragged-M tile.
+template <int KIND>
+__device__ __forceinline__ void prefetch_b(const CUtensorMap *tmB, const Tile &t, int kb) {
+  const int k0 = kb * BK;
+  if (KIND == GATE_UP) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_prefetch_4d(tmB, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
+  } else if (KIND == DOWN) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_prefetch_3d(tmB, t.n0 + 64 * i, k0, t.e);
+  } else if (KIND == DGRAD_H || KIND == DGRAD_X) {
+    tma_prefetch_3d(tmB, k0, t.n0, t.e);
   }
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const Args a) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO,
+                        const __grid_constant__ CUtensorMap tmO2, const Args a) {
   constexpr int A_MN = (KIND == WGRAD) ? 1 : 0;
   constexpr int B_MN = (KIND == DGRAD_H || KIND == DGRAD_X) ? 0 : 1;
   constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
@@ -259,13 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 1);
-      mbar_init(&acce_bar[b], 4);
+      mbar_init(&acce_bar[b], kEpiWarps);
     }
     mbar_init(&drain_bar, 1);
     fence_barrier_init();
     fence_proxy_async_shared();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmO);
+    if (KIND == GATE_UP) tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, kTmemCols);
@@ -284,6 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       int issued = 0;
+      // ragged-M kinds have the same K for every tile, so the i-th k-block of this
+      // CTA's stream is (tile blockIdx.x + (i / kt) * gridDim.x, k-block i % kt); the
+      // weight tiles of stream position i + kPrefetch go to L2 while position i loads.
+      int pf_local = -1;  // the stream tile last decoded for prefetching
+      Tile pf_t{};
+      auto prefetch_at = [&](int i) {
+        if (KIND == WGRAD || kPrefetch == 0 || a.k_tiles == 0) return;
+        const int local = i / a.k_tiles;
+        const int tile = blockIdx.x + local * gridDim.x;
+        if (tile >= total) return;
+        if (local != pf_local) {
+          pf_local = local;
+          pf_t = decode<KIND>(a, tile);
+        }
+        prefetch_b<KIND>(&tmB, pf_t, i - local * a.k_tiles);
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch_at(i);
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode<KIND>(a, tile);
         for (int kb = 0; kb < t.kt; ++kb) {
@@ -294,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *sA = smem + s * kStageBytes;
           mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
           issue_loads<KIND>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], t, kb);
+          prefetch_at(issued + kPrefetch);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -370,24 +498,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int ch = (warp - 2) >> 2;  // which half of the tile's columns it handles
+    Stager st{smem + kStages * kStageBytes + (warp - 2) * 2 * kStageOutBytes, 0};
     int buf = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode<KIND>(a, tile);
+      if (KIND == DGRAD_H) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
       bool ok = mbar_wait(&accf_bar[buf], aph, a.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
-      epilogue_tile<KIND>(a, t, taddr, row_in_tile);
+      epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[buf]);
       buf ^= 1;
       if (buf == 0) aph ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // the staged stores have left smem and landed
   }
 
   __syncwarp();
@@ -404,8 +535,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap &tmA, const CUtensorMap &tmB, const Args &a,
-                        int64_t max_tiles, const char *name, cudaStream_t st) {
+cudaError_t launch_kind(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO,
+                        const CUtensorMap &tmO2, const Args &a, int64_t max_tiles,
+                        const char *name, cudaStream_t st) {
   static bool attr_set[64] = {};  // per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -418,26 +550,37 @@ cudaError_t launch_kind(const CUtensorMap &tmA, const CUtensorMap &tmB, const Ar
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
   launch_begin(st);
-  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmO, tmO2, a);
   return note_launch(name, st);
 }
 
 inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Operand maps use 64-column boxes with the 128-byte swizzle; output maps (TMA
+// stores from the epilogue staging) use 32-column boxes with the 64-byte swizzle.
 cudaError_t map2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                  uint32_t box_rows) {
+                  uint32_t box_rows, int swizzle = 128) {
   const uint64_t dims[2] = {inner, rows};
   const uint64_t strides[1] = {inner * 2};
   const uint32_t box[2] = {box_inner, box_rows};
-  return encode_tensor_map(m, base, 2, dims, strides, box);
+  return encode_tensor_map(m, base, 2, dims, strides, box, swizzle);
 }
 
 cudaError_t map3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer,
-                  uint32_t box_inner, uint32_t box_mid) {
+                  uint32_t box_inner, uint32_t box_mid, int swizzle = 128) {
   const uint64_t dims[3] = {inner, mid, outer};
   const uint64_t strides[2] = {inner * 2, inner * mid * 2};
   const uint32_t box[3] = {box_inner, box_mid, 1};
-  return encode_tensor_map(m, base, 3, dims, strides, box);
+  return encode_tensor_map(m, base, 3, dims, strides, box, swizzle);
+}
+
+// [outer][2][inner] viewed as 3-D with one 32-row slab of one half per box: the
+// gate|up layout of GU and dGU (inner = f).
+cudaError_t map_halves(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
+  const uint64_t dims[3] = {inner, 2, rows};
+  const uint64_t strides[2] = {inner * 2, inner * 4};
+  const uint32_t box[3] = {32, 1, 32};
+  return encode_tensor_map(m, base, 3, dims, strides, box, 64);
 }
 
 Args base_args(const GemmPlan &p, int *status) {
@@ -452,7 +595,7 @@ Args base_args(const GemmPlan &p, int *status) {
 }  // namespace
 
 cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                              const uint64_t *strides_bytes, const uint32_t *box) {
+                              const uint64_t *strides_bytes, const uint32_t *box, int swizzle) {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -473,7 +616,8 @@ cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, cons
   }
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                         const_cast<void *>(base), gdim, gstride, bdim, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -493,93 +637,97 @@ int num_sms() {
 
 cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, void *h, void *gu,
                          int d, int f, int *status, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO, tO2;
   cudaError_t e = map2d(&tA, xp, d, p.R, 64, BM);
   if (e != cudaSuccess) return e;
   {
     const uint64_t dims[4] = {(uint64_t)f, 2, (uint64_t)d, (uint64_t)p.E};
     const uint64_t strides[3] = {(uint64_t)f * 2, (uint64_t)f * 4, (uint64_t)d * f * 4};
     const uint32_t box[4] = {64, 1, 64, 1};
-    e = encode_tensor_map(&tB, w_gu, 4, dims, strides, box);
+    e = encode_tensor_map(&tB, w_gu, 4, dims, strides, box, 128);
     if (e != cudaSuccess) return e;
   }
+  e = map2d(&tO, h, f, p.R, 32, 32, 64);
+  if (e != cudaSuccess) return e;
+  e = gu ? map_halves(&tO2, gu, f, p.R) : map2d(&tO2, h, f, p.R, 32, 32, 64);
+  if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN / 2);
   a.k_tiles = cdiv(d, BK);
   a.N_out = f;
   a.f = f;
-  a.out = h;
-  a.ld_out = f;
   a.out2 = gu;
-  a.ld_out2 = 2 * (int64_t)f;
-  return launch_kind<GATE_UP>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_gate_up_swiglu", st);
+  return launch_kind<GATE_UP>(tA, tB, tO, tO2, a, (p.R / BM) * a.n_tiles, "gemm_gate_up_swiglu",
+                              st);
 }
 
 cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void *o, int d, int f,
                       int *status, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO;
   cudaError_t e = map2d(&tA, h, f, p.R, 64, BM);
   if (e != cudaSuccess) return e;
   e = map3d(&tB, w_down, d, f, p.E, 64, 64);
+  if (e != cudaSuccess) return e;
+  e = map2d(&tO, o, d, p.R, 32, 32, 64);
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
   a.k_tiles = cdiv(f, BK);
   a.N_out = d;
-  a.out = o;
-  a.ld_out = d;
-  return launch_kind<DOWN>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_down", st);
+  return launch_kind<DOWN>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles, "gemm_down", st);
 }
 
 cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, const void *gu,
                          void *dgu, int d, int f, int *status, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO;
   cudaError_t e = map2d(&tA, g, d, p.R, 64, BM);
   if (e != cudaSuccess) return e;
   e = map3d(&tB, w_down, d, f, p.E, 64, BN);  // [E][f][d]: K = d inner, N = f rows
+  if (e != cudaSuccess) return e;
+  e = map_halves(&tO, dgu, f, p.R);
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN);
   a.k_tiles = cdiv(d, BK);
   a.N_out = f;
   a.f = f;
-  a.out = dgu;
-  a.ld_out = 2 * (int64_t)f;
   a.aux = gu;
   a.ld_aux = 2 * (int64_t)f;
-  return launch_kind<DGRAD_H>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_h_swiglu_bwd", st);
+  return launch_kind<DGRAD_H>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles,
+                              "gemm_dgrad_h_swiglu_bwd", st);
 }
 
 cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, void *dxp, int d,
                          int f, int *status, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO;
   cudaError_t e = map2d(&tA, dgu, 2 * (uint64_t)f, p.R, 64, BM);
   if (e != cudaSuccess) return e;
   e = map3d(&tB, w_gu, 2 * (uint64_t)f, d, p.E, 64, BN);  // [E][d][2f]: K = 2f inner, N = d rows
+  if (e != cudaSuccess) return e;
+  e = map2d(&tO, dxp, d, p.R, 32, 32, 64);
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
   a.k_tiles = cdiv(2 * (int64_t)f, BK);
   a.N_out = d;
-  a.out = dxp;
-  a.ld_out = d;
-  return launch_kind<DGRAD_X>(tA, tB, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_x", st);
+  return launch_kind<DGRAD_X>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_x", st);
 }
 
 cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
                        int *status, const char *name, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO;
   cudaError_t e = map2d(&tA, x, M, p.R, 64, 64);
   if (e != cudaSuccess) return e;
   e = map2d(&tB, y, N, p.R, 64, 64);
+  if (e != cudaSuccess) return e;
+  e = map3d(&tO, dw, N, M, p.E, 32, 32, 64);
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.m_tiles = cdiv(M, BM);
   a.n_tiles = cdiv(N, BN);
   a.M_out = M;
   a.N_out = N;
-  a.out = dw;
-  return launch_kind<WGRAD>(tA, tB, a, (int64_t)p.E * a.m_tiles * a.n_tiles, name, st);
+  return launch_kind<WGRAD>(tA, tB, tO, tO, a, (int64_t)p.E * a.m_tiles * a.n_tiles, name, st);
 }
 
 }  // namespace moe

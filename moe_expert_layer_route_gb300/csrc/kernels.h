@@ -72,9 +72,10 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
 cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
                        int *status, const char *name, cudaStream_t st);
 
-// Driver entry point for cuTensorMapEncodeTiled (resolved once).
+// cuTensorMapEncodeTiled through the driver entry point (resolved once): bf16
+// elements, zero fill out of bounds, swizzle 128 or 64 (bytes).
 cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                              const uint64_t *strides_bytes, const uint32_t *box);
+                              const uint64_t *strides_bytes, const uint32_t *box, int swizzle);
 
 int num_sms();
 
