@@ -38,12 +38,11 @@ constexpr int kTmemCols = 512;
 constexpr int kStageOutBytes = 32 * 32 * 2;
 constexpr int kEpiSmem = kEpiWarps * 2 * kStageOutBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + kEpiSmem + 1024;
-#ifndef MOE_GEMM_PREFETCH
-#define MOE_GEMM_PREFETCH 0
-#endif
-// k-blocks of weight tiles prefetched into L2 ahead of the smem ring (0 = off; on
-// GB300 every distance tried, 4 and 8, made the ragged-M GEMMs slower)
-constexpr int kPrefetch = MOE_GEMM_PREFETCH;
+// Ragged-M tile order (see decode): weight-stationary when experts have few rows
+// (each weight tile is then shared by only a few CTAs, which should run together),
+// m-tile major when they have many (the activation rows are then the reused operand).
+// Measured on GB300: weight-stationary is faster at 512 rows per expert, m-major at 8192.
+constexpr int64_t kWeightStationaryMaxRows = 2048;
 
 enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
 
@@ -54,6 +53,7 @@ struct Args {
   int n_tiles;  // tiles along N
   int m_tiles;  // WGRAD: tiles along M of one expert's dW
   int k_tiles;  // ragged-M kinds: K / 64, rounded up
+  int weight_stationary;  // ragged-M tile order
   int M_out;    // WGRAD: rows of dW[e]
   int N_out;    // valid output columns
   int f;        // SwiGLU width (GATE_UP, DGRAD_H)
@@ -85,9 +85,23 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile) {
     t.kr0 = a.padded[t.e];
     t.kt = (a.padded[t.e + 1] - t.kr0) / BK;
   } else {
-    const int mt = tile / a.n_tiles;
-    const int nt = tile - mt * a.n_tiles;
-    t.e = a.tile_expert[mt];
+    int mt, nt;
+    if (!a.weight_stationary) {
+      // m-tile major: consecutive tiles share the activation rows
+      mt = tile / a.n_tiles;
+      nt = tile - mt * a.n_tiles;
+      t.e = a.tile_expert[mt];
+    } else {
+      // weight-stationary: within an expert, (n-tile, m-tile) with m fastest, so the
+      // CTAs that read one weight tile run together. Expert e owns tiles
+      // [n_tiles * P_e / 128, n_tiles * P_(e+1) / 128).
+      t.e = a.tile_expert[tile / a.n_tiles];
+      const int base = a.padded[t.e] / BM;
+      const int mtiles = a.padded[t.e + 1] / BM - base;
+      const int local = tile - base * a.n_tiles;
+      nt = local / mtiles;
+      mt = base + (local - nt * mtiles);
+    }
     t.m0 = mt * BM;
     t.n0 = nt * (KIND == GATE_UP ? BN / 2 : BN);
     t.kt = a.k_tiles;
@@ -322,21 +336,6 @@ __device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, in
   }
 }
 
-// L2 prefetch of the weight (B) tiles of one k-block of a ragged-M tile.
-template <int KIND>
-__device__ __forceinline__ void prefetch_b(const CUtensorMap *tmB, const Tile &t, int kb) {
-  const int k0 = kb * BK;
-  if (KIND == GATE_UP) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tma_prefetch_4d(tmB, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
-  } else if (KIND == DOWN) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tma_prefetch_3d(tmB, t.n0 + 64 * i, k0, t.e);
-  } else if (KIND == DGRAD_H || KIND == DGRAD_X) {
-    tma_prefetch_3d(tmB, k0, t.n0, t.e);
-  }
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -394,23 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       int issued = 0;
-      // ragged-M kinds have the same K for every tile, so the i-th k-block of this
-      // CTA's stream is (tile blockIdx.x + (i / kt) * gridDim.x, k-block i % kt); the
-      // weight tiles of stream position i + kPrefetch go to L2 while position i loads.
-      int pf_local = -1;  // the stream tile last decoded for prefetching
-      Tile pf_t{};
-      auto prefetch_at = [&](int i) {
-        if (KIND == WGRAD || kPrefetch == 0 || a.k_tiles == 0) return;
-        const int local = i / a.k_tiles;
-        const int tile = blockIdx.x + local * gridDim.x;
-        if (tile >= total) return;
-        if (local != pf_local) {
-          pf_local = local;
-          pf_t = decode<KIND>(a, tile);
-        }
-        prefetch_b<KIND>(&tmB, pf_t, i - local * a.k_tiles);
-      };
-      for (int i = 0; i < kPrefetch; ++i) prefetch_at(i);
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode<KIND>(a, tile);
         for (int kb = 0; kb < t.kt; ++kb) {
@@ -421,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *sA = smem + s * kStageBytes;
           mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
           issue_loads<KIND>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], t, kb);
-          prefetch_at(issued + kPrefetch);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -589,6 +570,7 @@ Args base_args(const GemmPlan &p, int *status) {
   a.tile_expert = p.tile_expert;
   a.E = p.E;
   a.status = status;
+  a.weight_stationary = p.rows_per_expert <= kWeightStationaryMaxRows;
   return a;
 }
 

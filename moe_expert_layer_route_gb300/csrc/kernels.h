@@ -57,6 +57,7 @@ struct GemmPlan {
   const int32_t *tile_expert;  // [R/128] expert of each 128-row tile
   int E;
   int64_t R;                   // rows of the padded space
+  int64_t rows_per_expert;     // T*k / E, the mean segment length (picks the tile order)
 };
 
 cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, void *h, void *gu,

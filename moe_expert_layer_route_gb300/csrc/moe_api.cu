@@ -260,7 +260,7 @@ moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
   MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, st));
-  const GemmPlan p{padded, tiles, (int)s.E, padded_rows(s)};
+  const GemmPlan p{padded, tiles, (int)s.E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, (int)s.d, (int)s.f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, (int)s.d, (int)s.f, status, st));
   return MOE_OK;
@@ -301,7 +301,7 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
                           (int)padded_rows(s), st));
-  const GemmPlan p{padded, tiles, E, padded_rows(s)};
+  const GemmPlan p{padded, tiles, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));
   MOE_CUDA(launch_combine(o, w, row_of, y, T, d, k, st));
@@ -329,7 +329,7 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   const void *xp = at<void>(fws, L.xp), *gu = at<void>(fws, L.gu), *h = at<void>(fws, L.h);
   int *status = at<int>(scratch, B.status);
   void *g = at<void>(scratch, B.g), *dgu = at<void>(scratch, B.dgu), *dxp = at<void>(scratch, B.dxp);
-  const GemmPlan p{padded, tiles, E, padded_rows(s)};
+  const GemmPlan p{padded, tiles, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, st));
   MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));
