@@ -24,11 +24,22 @@
 namespace moe {
 namespace {
 
+// Two forms of the engine, chosen per launch. Single: one CTA per 128 x 256 tile.
+// Pair: two SMs (a 2-CTA cluster) share one 256 x 256 tile through the cta_group::2
+// MMA: each CTA loads its own 128 rows of A and half of the B tile, the even CTA
+// issues the MMA, and each CTA keeps its 128 rows of the accumulator in its TMEM. Per
+// CTA a k-block then moves 32 KB instead of 48 KB, which leaves room for 6 stages.
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kMTile = PAIR ? 2 * BM : BM;  // rows of one (pair-)tile
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows (N) each CTA loads
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBBytes = kBRows * BK * 2;    // 16 or 32 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+};
 constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box (MN-major tiles are built of these)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -37,7 +48,13 @@ constexpr int kTmemCols = 512;
 // 64-byte swizzled like the TMA store expects)
 constexpr int kStageOutBytes = 32 * 32 * 2;
 constexpr int kEpiSmem = kEpiWarps * 2 * kStageOutBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + kEpiSmem + 1024;
+template <bool PAIR>
+constexpr int smem_bytes() {
+  return Cfg<PAIR>::kStages * Cfg<PAIR>::kStageBytes + kEpiSmem + 1024;
+}
+// ragged-M GEMMs run on pairs when experts average at least this many rows (at 256
+// rows an odd tile count per expert wastes too many half-pairs)
+constexpr int64_t kPairMinRows = 384;
 // Ragged-M tile order (see decode): weight-stationary when experts have few rows
 // (each weight tile is then shared by only a few CTAs, which should run together),
 // m-tile major when they have many (the activation rows are then the reused operand).
@@ -49,9 +66,11 @@ enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
 struct Args {
   const int32_t *padded;       // [E+1]
   const int32_t *tile_expert;  // [R/128]
+  const int32_t *pair_start;   // [E+1] (pair mode)
+  const int32_t *pair_expert;  // pair-tile -> expert (pair mode)
   int E;
   int n_tiles;  // tiles along N
-  int m_tiles;  // WGRAD: tiles along M of one expert's dW
+  int m_tiles;  // WGRAD: (pair-)tiles along M of one expert's dW
   int k_tiles;  // ragged-M kinds: K / 64, rounded up
   int weight_stationary;  // ragged-M tile order
   int M_out;    // WGRAD: rows of dW[e]
@@ -63,81 +82,118 @@ struct Args {
   int *status;
 };
 
+// One CTA's share of a (pair-)tile: its 128 rows start at m0; valid is false when a
+// pair-tile's second 128-row block lies past the expert's segment (its rows then
+// feed the MMA but nothing is stored).
 struct Tile {
   int e, m0, n0, kt, kr0;
+  bool valid;
 };
 
-template <int KIND>
+template <int KIND, bool PAIR>
 __device__ __forceinline__ int total_tiles(const Args &a) {
   if (KIND == WGRAD) return a.E * a.m_tiles * a.n_tiles;
+  if (PAIR) return a.pair_start[a.E] * a.n_tiles;
   return (a.padded[a.E] / BM) * a.n_tiles;
 }
 
-template <int KIND>
-__device__ __forceinline__ Tile decode(const Args &a, int tile) {
+template <int KIND, bool PAIR>
+__device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
+  constexpr int kMTile = Cfg<PAIR>::kMTile;
   Tile t;
+  t.valid = true;
   if (KIND == WGRAD) {
     const int per = a.m_tiles * a.n_tiles;
     t.e = tile / per;
     const int r = tile - t.e * per;
-    t.m0 = (r / a.n_tiles) * BM;
+    t.m0 = (r / a.n_tiles) * kMTile + rank * BM;
     t.n0 = (r % a.n_tiles) * BN;
     t.kr0 = a.padded[t.e];
     t.kt = (a.padded[t.e + 1] - t.kr0) / BK;
-  } else {
-    int mt, nt;
-    if (!a.weight_stationary) {
-      // m-tile major: consecutive tiles share the activation rows
-      mt = tile / a.n_tiles;
-      nt = tile - mt * a.n_tiles;
-      t.e = a.tile_expert[mt];
-    } else {
-      // weight-stationary: within an expert, (n-tile, m-tile) with m fastest, so the
-      // CTAs that read one weight tile run together. Expert e owns tiles
-      // [n_tiles * P_e / 128, n_tiles * P_(e+1) / 128).
-      t.e = a.tile_expert[tile / a.n_tiles];
-      const int base = a.padded[t.e] / BM;
-      const int mtiles = a.padded[t.e + 1] / BM - base;
-      const int local = tile - base * a.n_tiles;
-      nt = local / mtiles;
-      mt = base + (local - nt * mtiles);
-    }
-    t.m0 = mt * BM;
-    t.n0 = nt * (KIND == GATE_UP ? BN / 2 : BN);
-    t.kt = a.k_tiles;
-    t.kr0 = 0;
+    return t;
   }
+  // ragged M: "units" are 128-row tiles (single) or pairs of them (pair mode);
+  // unit_start[e] / unit_expert[u] locate them.
+  int u, nt;
+  if (!a.weight_stationary) {
+    // unit major: consecutive tiles share the activation rows
+    u = tile / a.n_tiles;
+    nt = tile - u * a.n_tiles;
+    t.e = PAIR ? a.pair_expert[u] : a.tile_expert[u];
+  } else {
+    // weight-stationary: within an expert, (n-tile, unit) with the unit fastest, so
+    // the CTAs that read one weight tile run together. Expert e owns tiles
+    // [n_tiles * start_e, n_tiles * start_(e+1)).
+    t.e = PAIR ? a.pair_expert[tile / a.n_tiles] : a.tile_expert[tile / a.n_tiles];
+    const int base = PAIR ? a.pair_start[t.e] : a.padded[t.e] / BM;
+    const int units = (PAIR ? a.pair_start[t.e + 1] : a.padded[t.e + 1] / BM) - base;
+    const int local = tile - base * a.n_tiles;
+    nt = local / units;
+    u = base + (local - nt * units);
+  }
+  int mt = u;
+  if (PAIR) {
+    mt = a.padded[t.e] / BM + 2 * (u - a.pair_start[t.e]) + rank;
+    t.valid = mt < a.padded[t.e + 1] / BM;
+  }
+  t.m0 = mt * BM;
+  t.n0 = nt * (KIND == GATE_UP ? BN / 2 : BN);
+  t.kt = a.k_tiles;
+  t.kr0 = 0;
   return t;
 }
 
-template <int KIND>
+// The loads of one k-block into this CTA's stage. Single: everything, completing on
+// the local barrier. Pair: this CTA's A rows and its half of B, completing on the
+// even CTA's barrier (bar_pair, a shared::cluster address).
+template <int KIND, bool PAIR>
 __device__ __forceinline__ void issue_loads(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                             uint8_t *sA, uint8_t *sB, uint64_t *bar,
-                                            const Tile &t, int kb) {
+                                            uint32_t bar_pair, const Tile &t, int kb, int rank) {
+  constexpr bool kPair = PAIR;
+  constexpr int kBRows = Cfg<PAIR>::kBRows;
   const int k0 = kb * BK;
-  // A operand
+  auto ld2 = [&](void *dst, const CUtensorMap *m, int c0, int c1) {
+    if (kPair) tma_load_2d_pair(dst, m, bar_pair, c0, c1);
+    else tma_load_2d(dst, m, bar, c0, c1);
+  };
+  auto ld3 = [&](void *dst, const CUtensorMap *m, int c0, int c1, int c2) {
+    if (kPair) tma_load_3d_pair(dst, m, bar_pair, c0, c1, c2);
+    else tma_load_3d(dst, m, bar, c0, c1, c2);
+  };
+  auto ld4 = [&](void *dst, const CUtensorMap *m, int c0, int c1, int c2, int c3) {
+    if (kPair) tma_load_4d_pair(dst, m, bar_pair, c0, c1, c2, c3);
+    else tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  };
+  // A operand: this CTA's 128 rows
   if (KIND == WGRAD) {
     // X^T tile: columns m0..m0+127 of X, rows kr0+k0 .. +63 (MN-major)
-    tma_load_2d(sA, tmA, bar, t.m0, t.kr0 + k0);
-    tma_load_2d(sA + kBoxBytes, tmA, bar, t.m0 + 64, t.kr0 + k0);
+    ld2(sA, tmA, t.m0, t.kr0 + k0);
+    ld2(sA + kBoxBytes, tmA, t.m0 + 64, t.kr0 + k0);
   } else {
-    tma_load_2d(sA, tmA, bar, k0, t.m0);  // rows m0..m0+127, K columns k0..k0+63
+    ld2(sA, tmA, k0, t.m0);  // rows m0..m0+127, K columns k0..k0+63
   }
-  // B operand
+  // B operand: N columns [n_lo, n_lo + kBRows) of the tile
   if (KIND == GATE_UP) {
-    // W_gu viewed as [E][d][2][f]: gate columns n0..n0+127 then up columns n0..n0+127
+    // W_gu viewed as [E][d][2][f]: the tile's N = 128 gate columns then the same 128
+    // up columns; a pair splits them, the even CTA loading gate and the odd one up
+    if (kPair) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_4d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
+      for (int i = 0; i < 2; ++i) ld4(sB + i * kBoxBytes, tmB, t.n0 + 64 * i, rank, k0, t.e);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ld4(sB + i * kBoxBytes, tmB, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
+    }
   } else if (KIND == DOWN) {
+    const int n_lo = t.n0 + rank * kBRows;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tma_load_3d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * i, k0, t.e);
+    for (int i = 0; i < kBRows / 64; ++i) ld3(sB + i * kBoxBytes, tmB, n_lo + 64 * i, k0, t.e);
   } else if (KIND == DGRAD_H || KIND == DGRAD_X) {
-    tma_load_3d(sB, tmB, bar, k0, t.n0, t.e);  // 256 N-rows x 64 K, K-major
+    ld3(sB, tmB, k0, t.n0 + rank * kBRows, t.e);  // kBRows N-rows x 64 K, K-major
   } else {
+    const int n_lo = t.n0 + rank * kBRows;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_2d(sB + i * kBoxBytes, tmB, bar, t.n0 + 64 * i, t.kr0 + k0);
+    for (int i = 0; i < kBRows / 64; ++i) ld2(sB + i * kBoxBytes, tmB, n_lo + 64 * i, t.kr0 + k0);
   }
 }
 
@@ -336,15 +392,19 @@ __device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, in
   }
 }
 
-template <int KIND>
+// Launched with a cluster of 2 when PAIR (see launch_kind).
+template <int KIND, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Args a) {
+  constexpr bool kPair = PAIR;
+  constexpr int kStages = Cfg<PAIR>::kStages, kStageBytes = Cfg<PAIR>::kStageBytes;
+  constexpr int kMTile = Cfg<PAIR>::kMTile;
   constexpr int A_MN = (KIND == WGRAD) ? 1 : 0;
   constexpr int B_MN = (KIND == DGRAD_H || KIND == DGRAD_X) ? 0 : 1;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kMTile, BN, A_MN, B_MN);
   // descriptor strides: K-major SW128 tiles use SBO = 1024 (8 rows of 128 B) and step
   // 32 B per 16-element K slice; MN-major SW128 tiles use LBO = one 64x64 box (the
   // next 64 M/N columns), SBO = 1024 (8 K rows) and step 16 rows = 2048 B per K slice.
@@ -359,14 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = kPair ? (int)cluster_ctarank() : 0;     // 0 = the CTA issuing MMAs
+  const int unit0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // this pair's first tile
+  const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&full_bar[s], 1);   // the even CTA's producer; bytes from both CTAs
+      mbar_init(&empty_bar[s], 1);  // one (multicast) commit per consumed stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 1);
-      mbar_init(&acce_bar[b], kEpiWarps);
+      mbar_init(&acce_bar[b], kPair ? 2 * kEpiWarps : kEpiWarps);  // both CTAs' epilogues
     }
     mbar_init(&drain_bar, 1);
     fence_barrier_init();
@@ -377,14 +440,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (KIND == GATE_UP) tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
-  const int total = total_tiles<KIND>(a);
+  const int total = total_tiles<KIND, PAIR>(a);
+  bool failed = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -393,16 +463,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       int issued = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode<KIND>(a, tile);
+      for (int tile = unit0; tile < total && ok; tile += units) {
+        const Tile t = decode<KIND, PAIR>(a, tile, rank);
         for (int kb = 0; kb < t.kt; ++kb) {
           if (!mbar_wait(&empty_bar[s], ph ^ 1, a.status)) {
             ok = false;
             break;
           }
           uint8_t *sA = smem + s * kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-          issue_loads<KIND>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], t, kb);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], (kPair ? 2 : 1) * kStageBytes);
+          const uint32_t bar_pair = kPair ? mapa_shared(&full_bar[s], 0) : 0;
+          issue_loads<KIND, PAIR>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], bar_pair, t, kb, rank);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -411,21 +482,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        // wait (bounded) for the copies this thread issued and that may be in flight
-        int n = issued < kStages ? issued : kStages;
-        int ss = s;
-        uint32_t pp = ph;
-        for (int i = 0; i < n; ++i) {
-          if (--ss < 0) {
-            ss = kStages - 1;
-            pp ^= 1;
+        failed = true;
+        if (rank == 0) {
+          // wait (bounded) for the copies in flight: the even CTA's full barriers
+          // count the bytes of both CTAs
+          int n = issued < kStages ? issued : kStages;
+          int ss = s;
+          uint32_t pp = ph;
+          for (int i = 0; i < n; ++i) {
+            if (--ss < 0) {
+              ss = kStages - 1;
+              pp ^= 1;
+            }
+            mbar_wait(&full_bar[ss], pp, nullptr, 100000000ull);
           }
-          mbar_wait(&full_bar[ss], pp, nullptr, 100000000ull);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // -------------------------------------------------------------- MMA issuer
       int s = 0;
       uint32_t ph = 0;
@@ -433,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aph = 0;
       bool ok = true, any = false;
       const uint32_t smem_base = smem_u32(smem);
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode<KIND>(a, tile);
+      for (int tile = unit0; tile < total && ok; tile += units) {
+        const Tile t = decode<KIND, PAIR>(a, tile, 0);
         if (!mbar_wait(&acce_bar[buf], aph ^ 1, a.status)) {
           ok = false;
           break;
@@ -442,7 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         if (t.kt == 0) {
+          // nothing to accumulate (an expert without rows): release the epilogues
           mbar_arrive(&accf_bar[buf]);
+          if (kPair) mbar_arrive_cluster(mapa_shared(&accf_bar[buf], 1));
         } else {
           for (int kb = 0; kb < t.kt; ++kb) {
             if (!mbar_wait(&full_bar[s], ph, a.status)) {
@@ -456,25 +533,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
-              tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+              if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+              else tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
             }
             any = true;
-            tc_commit(&empty_bar[s]);
+            if (kPair) tc_commit_pair(&empty_bar[s]);
+            else tc_commit(&empty_bar[s]);
             if (++s == kStages) {
               s = 0;
               ph ^= 1;
             }
           }
           if (!ok) break;
-          tc_commit(&accf_bar[buf]);
+          if (kPair) tc_commit_pair(&accf_bar[buf]);
+          else tc_commit(&accf_bar[buf]);
         }
         buf ^= 1;
         if (buf == 0) aph ^= 1;
       }
-      if (!ok && any) {
-        // let every issued MMA finish before the accumulator is freed
-        tc_commit(&drain_bar);
-        mbar_wait(&drain_bar, 0, nullptr, 100000000ull);
+      if (!ok) {
+        failed = true;
+        if (any) {
+          // let every issued MMA finish before the accumulator is freed
+          if (kPair) tc_commit_pair(&drain_bar);
+          else tc_commit(&drain_bar);
+          mbar_wait(&drain_bar, 0, nullptr, 100000000ull);
+        }
       }
     }
   } else {
@@ -482,20 +566,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int ch = (warp - 2) >> 2;  // which half of the tile's columns it handles
     Stager st{smem + kStages * kStageBytes + (warp - 2) * 2 * kStageOutBytes, 0};
+    const uint32_t acce_pair0 = kPair ? mapa_shared(&acce_bar[0], 0) : 0;
+    const uint32_t acce_pair1 = kPair ? mapa_shared(&acce_bar[1], 0) : 0;
     int buf = 0;
     uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode<KIND>(a, tile);
-      if (KIND == DGRAD_H) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
+    for (int tile = unit0; tile < total; tile += units) {
+      const Tile t = decode<KIND, PAIR>(a, tile, rank);
+      if (KIND == DGRAD_H && t.valid) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
       bool ok = mbar_wait(&accf_bar[buf], aph, a.status);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      if (!ok) {
+        failed = true;
+        break;
+      }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
-      epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2);
+      if (t.valid) epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[buf]);
+      if (lane == 0) {
+        if (kPair) mbar_arrive_cluster(buf ? acce_pair1 : acce_pair0);
+        else mbar_arrive(&acce_bar[buf]);
+      }
       buf ^= 1;
       if (buf == 0) aph ^= 1;
     }
@@ -503,11 +595,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncwarp();
+  if (__syncthreads_or(failed)) {
+    // a wait gave up: give copies that may still target this CTA's smem time to land
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+  }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // no signal or MMA of the pair still targets this CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -515,23 +614,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-template <int KIND>
-cudaError_t launch_kind(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO,
-                        const CUtensorMap &tmO2, const Args &a, int64_t max_tiles,
-                        const char *name, cudaStream_t st) {
+template <int KIND, bool PAIR>
+cudaError_t launch_kind_as(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO,
+                           const CUtensorMap &tmO2, const Args &a, int64_t max_tiles,
+                           const char *name, cudaStream_t st) {
   static bool attr_set[64] = {};  // per device
+  static int slots_cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
+  auto kernel = grouped_gemm_kernel<KIND, PAIR>;
   if (!attr_set[dev & 63]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes<PAIR>());
     if (e != cudaSuccess) return e;
     attr_set[dev & 63] = true;
   }
   if (max_tiles <= 0) return cudaSuccess;
-  const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = PAIR ? 2 : 1;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<PAIR>();
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  // persistent: as many CTAs (or CTA pairs) as can be resident at once, never more
+  // than there are tiles
+  int &slots = slots_cache[dev & 63];
+  if (slots == 0) {
+    slots = num_sms();
+    if (PAIR) {
+      cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+      int clusters = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters <= 0) return cudaErrorInvalidConfiguration;
+      slots = clusters;
+    }
+  }
+  cfg.gridDim = dim3((int)(max_tiles < slots ? max_tiles : slots) * (PAIR ? 2 : 1), 1, 1);
   launch_begin(st);
-  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, tmO, tmO2, a);
+  cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, tmO2, a);
   return note_launch(name, st);
 }
 
@@ -564,10 +690,28 @@ cudaError_t map_halves(CUtensorMap *m, const void *base, uint64_t inner, uint64_
   return encode_tensor_map(m, base, 3, dims, strides, box, 64);
 }
 
+// Upper bound of the ragged-M units (128-row tiles, or pairs of them in one expert).
+int64_t max_units(const GemmPlan &p, bool pair) {
+  return pair ? p.R / (2 * BM) + p.E : p.R / BM;
+}
+
+// pairs of SMs for the ragged-M GEMMs when experts are long enough (kPairMinRows)
+bool pair_for_rows(const GemmPlan &p) { return p.rows_per_expert >= kPairMinRows; }
+
+template <int KIND>
+cudaError_t launch_kind(bool pair, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const CUtensorMap &tmO, const CUtensorMap &tmO2, const Args &a,
+                        int64_t max_tiles, const char *name, cudaStream_t st) {
+  return pair ? launch_kind_as<KIND, true>(tmA, tmB, tmO, tmO2, a, max_tiles, name, st)
+              : launch_kind_as<KIND, false>(tmA, tmB, tmO, tmO2, a, max_tiles, name, st);
+}
+
 Args base_args(const GemmPlan &p, int *status) {
   Args a{};
   a.padded = p.padded;
   a.tile_expert = p.tile_expert;
+  a.pair_start = p.pair_start;
+  a.pair_expert = p.pair_expert;
   a.E = p.E;
   a.status = status;
   a.weight_stationary = p.rows_per_expert <= kWeightStationaryMaxRows;
@@ -639,8 +783,9 @@ cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, vo
   a.N_out = f;
   a.f = f;
   a.out2 = gu;
-  return launch_kind<GATE_UP>(tA, tB, tO, tO2, a, (p.R / BM) * a.n_tiles, "gemm_gate_up_swiglu",
-                              st);
+  const bool pair = pair_for_rows(p);
+  return launch_kind<GATE_UP>(pair, tA, tB, tO, tO2, a, max_units(p, pair) * a.n_tiles,
+                              "gemm_gate_up_swiglu", st);
 }
 
 cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void *o, int d, int f,
@@ -656,15 +801,19 @@ cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void
   a.n_tiles = cdiv(d, BN);
   a.k_tiles = cdiv(f, BK);
   a.N_out = d;
-  return launch_kind<DOWN>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles, "gemm_down", st);
+  const bool pair = pair_for_rows(p);
+  return launch_kind<DOWN>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles, "gemm_down",
+                           st);
 }
 
 cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, const void *gu,
                          void *dgu, int d, int f, int *status, cudaStream_t st) {
   CUtensorMap tA, tB, tO;
+  const bool pair = pair_for_rows(p);
   cudaError_t e = map2d(&tA, g, d, p.R, 64, BM);
   if (e != cudaSuccess) return e;
-  e = map3d(&tB, w_down, d, f, p.E, 64, BN);  // [E][f][d]: K = d inner, N = f rows
+  // [E][f][d]: K = d inner, N = f rows; each CTA of a pair loads half the N rows
+  e = map3d(&tB, w_down, d, f, p.E, 64, pair ? BN / 2 : BN);
   if (e != cudaSuccess) return e;
   e = map_halves(&tO, dgu, f, p.R);
   if (e != cudaSuccess) return e;
@@ -675,16 +824,18 @@ cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, c
   a.f = f;
   a.aux = gu;
   a.ld_aux = 2 * (int64_t)f;
-  return launch_kind<DGRAD_H>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles,
+  return launch_kind<DGRAD_H>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles,
                               "gemm_dgrad_h_swiglu_bwd", st);
 }
 
 cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, void *dxp, int d,
                          int f, int *status, cudaStream_t st) {
   CUtensorMap tA, tB, tO;
+  const bool pair = pair_for_rows(p);
   cudaError_t e = map2d(&tA, dgu, 2 * (uint64_t)f, p.R, 64, BM);
   if (e != cudaSuccess) return e;
-  e = map3d(&tB, w_gu, 2 * (uint64_t)f, d, p.E, 64, BN);  // [E][d][2f]: K = 2f inner, N = d rows
+  // [E][d][2f]: K = 2f inner, N = d rows; each CTA of a pair loads half the N rows
+  e = map3d(&tB, w_gu, 2 * (uint64_t)f, d, p.E, 64, pair ? BN / 2 : BN);
   if (e != cudaSuccess) return e;
   e = map2d(&tO, dxp, d, p.R, 32, 32, 64);
   if (e != cudaSuccess) return e;
@@ -692,7 +843,8 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
   a.n_tiles = cdiv(d, BN);
   a.k_tiles = cdiv(2 * (int64_t)f, BK);
   a.N_out = d;
-  return launch_kind<DGRAD_X>(tA, tB, tO, tO, a, (p.R / BM) * a.n_tiles, "gemm_dgrad_x", st);
+  return launch_kind<DGRAD_X>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles,
+                              "gemm_dgrad_x", st);
 }
 
 cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw, int M, int N,
@@ -705,11 +857,13 @@ cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw
   e = map3d(&tO, dw, N, M, p.E, 32, 32, 64);
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
-  a.m_tiles = cdiv(M, BM);
+  const bool pair = true;  // measured faster on pairs at 512 and 8192 rows per expert
+  a.m_tiles = cdiv(M, pair ? 2 * BM : BM);
   a.n_tiles = cdiv(N, BN);
   a.M_out = M;
   a.N_out = N;
-  return launch_kind<WGRAD>(tA, tB, tO, tO, a, (int64_t)p.E * a.m_tiles * a.n_tiles, name, st);
+  return launch_kind<WGRAD>(pair, tA, tB, tO, tO, a, (int64_t)p.E * a.m_tiles * a.n_tiles, name,
+                            st);
 }
 
 }  // namespace moe

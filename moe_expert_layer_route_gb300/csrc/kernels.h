@@ -22,10 +22,13 @@ cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *r
                          int32_t *hist, int T, int E, int k, bool with_count, cudaStream_t st);
 cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,
                          cudaStream_t st);
+// pair_start / pair_expert may be null (then only the 128-row tile table is written)
 cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
-                        int32_t *padded, int32_t *tile_expert, cudaStream_t st);
+                        int32_t *padded, int32_t *tile_expert, int32_t *pair_start,
+                        int32_t *pair_expert, cudaStream_t st);
 cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t *padded,
-                        int32_t *tile_expert, cudaStream_t st);
+                        int32_t *tile_expert, int32_t *pair_start, int32_t *pair_expert,
+                        cudaStream_t st);
 cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *rank,
                            const int32_t *hist, const int32_t *padded, const int32_t *counts,
                            int32_t *row_of, int32_t *tok_of, void *xp, int T, int d, int E, int k,
@@ -55,6 +58,8 @@ cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *
 struct GemmPlan {
   const int32_t *padded;       // [E+1] padded segment starts
   const int32_t *tile_expert;  // [R/128] expert of each 128-row tile
+  const int32_t *pair_start;   // [E+1] first 256-row pair-tile of each expert
+  const int32_t *pair_expert;  // [R/128] expert of each pair-tile
   int E;
   int64_t R;                   // rows of the padded space
   int64_t rows_per_expert;     // T*k / E, the mean segment length (picks the tile order)

@@ -16,8 +16,8 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct FwdLayout {
-  size_t status, ids, w, rank, hist, counts, offsets, padded, tile_expert, row_of, tok_of, xp, gu,
-      h, o, total;
+  size_t status, ids, w, rank, hist, counts, offsets, padded, tile_expert, pair_start, pair_expert,
+      row_of, tok_of, xp, gu, h, o, total;
 };
 
 struct BwdLayout {
@@ -48,6 +48,8 @@ FwdLayout fwd_layout(const moe_shape &s, int training) {
   L.offsets = take((s.E + 1) * 4);
   L.padded = take((s.E + 1) * 4);
   L.tile_expert = take(R / kTileRows * 4);
+  L.pair_start = take((s.E + 1) * 4);
+  L.pair_expert = take(R / kTileRows * 4);
   L.row_of = take(A * 4);
   L.tok_of = take(R * 4);
   L.xp = take((size_t)R * s.d * 2);
@@ -239,7 +241,7 @@ moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_
   int32_t *rank = at<int32_t>(ws, L.rank), *hist = at<int32_t>(ws, L.hist);
   MOE_CUDA(launch_count(ids, rank, hist, T, E, k, st));
   MOE_CUDA(launch_scan(hist, T, E, counts, offsets, padded_offsets, at<int32_t>(ws, L.tile_expert),
-                       st));
+                       nullptr, nullptr, st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded_offsets, counts, row_of, tok_of, xp, T, d, E,
                           k, (int)padded_rows(s), st));
   return MOE_OK;
@@ -259,8 +261,10 @@ moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts
   int *status = at<int>(ws, L.status);
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
-  MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, st));
-  const GemmPlan p{padded, tiles, (int)s.E, padded_rows(s), s.T * s.k / s.E};
+  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
+  MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
+                       st));
+  const GemmPlan p{padded, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, (int)s.d, (int)s.f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, (int)s.d, (int)s.f, status, st));
   return MOE_OK;
@@ -298,10 +302,12 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   void *gu = training ? at<void>(ws, L.gu) : nullptr;
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_route(logits, ids, w, rank, hist, T, E, k, true, st));
-  MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, st));
+  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
+  MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
+                       st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
                           (int)padded_rows(s), st));
-  const GemmPlan p{padded, tiles, E, padded_rows(s), s.T * s.k / s.E};
+  const GemmPlan p{padded, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));
   MOE_CUDA(launch_combine(o, w, row_of, y, T, d, k, st));
@@ -326,10 +332,11 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   const float *w = at<float>(fws, L.w);
   const int32_t *row_of = at<int32_t>(fws, L.row_of), *counts = at<int32_t>(fws, L.counts);
   const int32_t *padded = at<int32_t>(fws, L.padded), *tiles = at<int32_t>(fws, L.tile_expert);
+  const int32_t *pstart = at<int32_t>(fws, L.pair_start), *pexp = at<int32_t>(fws, L.pair_expert);
   const void *xp = at<void>(fws, L.xp), *gu = at<void>(fws, L.gu), *h = at<void>(fws, L.h);
   int *status = at<int>(scratch, B.status);
   void *g = at<void>(scratch, B.g), *dgu = at<void>(scratch, B.dgu), *dxp = at<void>(scratch, B.dxp);
-  const GemmPlan p{padded, tiles, E, padded_rows(s), s.T * s.k / s.E};
+  const GemmPlan p{padded, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, st));
   MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));

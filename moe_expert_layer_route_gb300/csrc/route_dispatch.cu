@@ -142,33 +142,49 @@ __global__ void __launch_bounds__(256) count_kernel(const int32_t *__restrict__ 
 // One block. Warp w scans the chunk counts of experts w, w+32, ... in chunk order,
 // turning hist[e][c] into the exclusive prefix within expert e; then the per-expert
 // totals give counts, compact offsets, padded offsets (segments rounded up to whole
-// 128-row tiles) and the table of which expert owns each 128-row tile.
+// 128-row tiles), the expert of every 128-row tile and, for the GEMMs that run on
+// pairs of SMs, the pairs of consecutive tiles of one expert: pair_start[e] is the
+// first pair of expert e (ceil(tiles_e / 2) pairs each) and pair_expert[p] the
+// expert of pair p. The pair tables are skipped when their pointers are null.
+__device__ int last_le(const int32_t *v, int n, int x) {  // last i < n with v[i] <= x
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (v[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __device__ void plan_from_counts(const int32_t *s_cnt, int E, int32_t *__restrict__ offsets,
                                  int32_t *__restrict__ padded, int32_t *__restrict__ tile_expert,
-                                 int32_t *s_pad) {
+                                 int32_t *__restrict__ pair_start,
+                                 int32_t *__restrict__ pair_expert, int32_t *s_pad,
+                                 int32_t *s_pair) {
   if (threadIdx.x == 0) {
-    int32_t off = 0, pad = 0;
+    int32_t off = 0, pad = 0, pairs = 0;
     for (int e = 0; e < E; ++e) {
       offsets[e] = off;
       padded[e] = pad;
       s_pad[e] = pad;
+      s_pair[e] = pairs;
+      const int tiles = (s_cnt[e] + kTileRows - 1) / kTileRows;
       off += s_cnt[e];
-      pad += (s_cnt[e] + kTileRows - 1) / kTileRows * kTileRows;
+      pad += tiles * kTileRows;
+      pairs += (tiles + 1) / 2;
     }
     offsets[E] = off;
     padded[E] = pad;
     s_pad[E] = pad;
+    s_pair[E] = pairs;
   }
   __syncthreads();
   const int ntiles = s_pad[E] / kTileRows;
-  for (int mt = threadIdx.x; mt < ntiles; mt += blockDim.x) {
-    const int row = mt * kTileRows;
-    int lo = 0, hi = E - 1;  // last e with s_pad[e] <= row
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_pad[mid] <= row) lo = mid; else hi = mid - 1;
-    }
-    tile_expert[mt] = lo;
+  for (int mt = threadIdx.x; mt < ntiles; mt += blockDim.x)
+    tile_expert[mt] = last_le(s_pad, E, mt * kTileRows);
+  if (pair_start) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) pair_start[e] = s_pair[e];
+    for (int p = threadIdx.x; p < s_pair[E]; p += blockDim.x)
+      pair_expert[p] = last_le(s_pair, E, p);
   }
 }
 
@@ -176,9 +192,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
                                                     int32_t *__restrict__ counts,
                                                     int32_t *__restrict__ offsets,
                                                     int32_t *__restrict__ padded,
-                                                    int32_t *__restrict__ tile_expert) {
+                                                    int32_t *__restrict__ tile_expert,
+                                                    int32_t *__restrict__ pair_start,
+                                                    int32_t *__restrict__ pair_expert) {
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ int32_t s_pad[kMaxE + 1];
+  __shared__ int32_t s_pair[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = warp; e < E; e += 32) {
     int32_t running = 0;
@@ -201,19 +220,22 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
     }
   }
   __syncthreads();
-  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, s_pad);
+  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, pair_start, pair_expert, s_pad, s_pair);
 }
 
 // The same plan from counts alone (standalone expert FFN calls).
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ counts, int E,
                                                     int32_t *__restrict__ offsets,
                                                     int32_t *__restrict__ padded,
-                                                    int32_t *__restrict__ tile_expert) {
+                                                    int32_t *__restrict__ tile_expert,
+                                                    int32_t *__restrict__ pair_start,
+                                                    int32_t *__restrict__ pair_expert) {
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ int32_t s_pad[kMaxE + 1];
+  __shared__ int32_t s_pair[kMaxE + 1];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = counts[e];
   __syncthreads();
-  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, s_pad);
+  plan_from_counts(s_cnt, E, offsets, padded, tile_expert, pair_start, pair_expert, s_pad, s_pair);
 }
 
 // ------------------------------------------------------------------------- scatter
@@ -377,17 +399,21 @@ cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T
 }
 
 cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
-                        int32_t *padded, int32_t *tile_expert, cudaStream_t st) {
+                        int32_t *padded, int32_t *tile_expert, int32_t *pair_start,
+                        int32_t *pair_expert, cudaStream_t st) {
   const int C = ceil_div(T, kChunk);
   launch_begin(st);
-  scan_kernel<<<1, 1024, 0, st>>>(hist, C, E, counts, offsets, padded, tile_expert);
+  scan_kernel<<<1, 1024, 0, st>>>(hist, C, E, counts, offsets, padded, tile_expert, pair_start,
+                                  pair_expert);
   return note_launch("scan", st);
 }
 
 cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t *padded,
-                        int32_t *tile_expert, cudaStream_t st) {
+                        int32_t *tile_expert, int32_t *pair_start, int32_t *pair_expert,
+                        cudaStream_t st) {
   launch_begin(st);
-  plan_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, padded, tile_expert);
+  plan_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, padded, tile_expert, pair_start,
+                                  pair_expert);
   return note_launch("plan", st);
 }
 

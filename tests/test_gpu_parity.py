@@ -48,6 +48,10 @@ FFN_CASES = [
     (256, 2048, 128, 8, 768, 14, False), # Qwen3-MoE-like widths, many near-empty experts
     (512, 256, 32, 4, 256, 15, True),    # skewed: empty experts, one expert gets every token
     (200, 128, 1, 1, 64, 16, False),     # E = 1: a dense SwiGLU MLP
+    # >= 384 rows per expert: the GEMMs run on SM pairs (256-row pair-tiles; an odd
+    # tile count leaves the second half of an expert's last pair-tile unused)
+    (1024, 256, 4, 2, 320, 17, False),
+    (900, 200, 3, 2, 200, 18, False),
 ]
 
 
@@ -155,6 +159,8 @@ BWD_CASES = [
     (96, 2880, 4, 2, 2880, 43, False),
     (200, 128, 1, 1, 64, 44, False),
     (1, 64, 4, 2, 64, 45, False),
+    (1024, 256, 4, 2, 320, 46, False),   # SM-pair GEMMs (see FFN_CASES)
+    (900, 200, 3, 2, 200, 47, False),
 ]
 
 
