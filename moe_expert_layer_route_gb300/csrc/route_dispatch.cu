@@ -15,6 +15,7 @@ namespace moe {
 constexpr int kChunk = 32;        // tokens per histogram chunk (one per lane of a warp)
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 256;
+constexpr int kVec = 4;           // 16-byte vectors each lane keeps in flight in the row copies
 
 // ---------------------------------------------------------------------------- route
 // One warp per token. Lane l holds logits l, l+32, ... (E <= 256, so <= 8 each).
@@ -92,10 +93,10 @@ __device__ __forceinline__ void count_chunk(const int32_t (*s_ids)[kMaxK], int c
   }
 }
 
-// Block c routes tokens [32c, 32c+32) with 8 warps and, when COUNT, also writes the
-// chunk histogram and local ranks for the dispatch.
+// Block c routes tokens [32c, 32c+32), one warp per token, and, when COUNT, also
+// writes the chunk histogram and local ranks for the dispatch.
 template <bool COUNT>
-__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits,
+__global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ logits,
                                                     int32_t *__restrict__ ids,
                                                     float *__restrict__ w,
                                                     int32_t *__restrict__ rank,
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
   __shared__ int32_t s_ids[kChunk][kMaxK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  for (int i = warp; i < kChunk; i += 8) {
+  for (int i = warp; i < kChunk; i += 32) {
     const int t = c * kChunk + i;
     if (t >= T) break;
     int sid;
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
   }
   if constexpr (COUNT) {
     __syncthreads();
-    count_chunk(s_ids, c, T, E, k, C, warp, 8, lane, rank, hist);
+    count_chunk(s_ids, c, T, E, k, C, warp, 32, lane, rank, hist);
   }
 }
 
@@ -264,12 +265,22 @@ __global__ void __launch_bounds__(256) scatter_kernel(
     int rows[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xffffffffu, row, j);
+    // kVec 16-byte loads in flight per lane, then their k stores each
     const uint4 *src = x + (int64_t)t * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(src + v);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kVec) {
+      uint4 val[kVec];
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < k) xp[(int64_t)rows[j] * nvec + v] = val;
+      for (int u = 0; u < kVec; ++u)
+        if (v0 + 32 * u < nvec) val[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          uint4 *dst = xp + (int64_t)rows[j] * nvec;
+#pragma unroll
+          for (int u = 0; u < kVec; ++u)
+            if (v0 + 32 * u < nvec) dst[v0 + 32 * u] = val[u];
+        }
+      }
     }
   } else if ((int)blockIdx.x < token_blocks + E) {
     const int e = blockIdx.x - token_blocks;
@@ -350,16 +361,26 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
       rows[j] = __shfl_sync(0xffffffffu, row, j);
       wts[j] = __shfl_sync(0xffffffffu, wt, j);
     }
-    for (int v = lane; v < nvec; v += 32) {
-      float f[8];
-      unpack8(__ldg(dy + (int64_t)t * nvec + v), f);
+    const uint4 *src = dy + (int64_t)t * nvec;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kVec) {
+      uint4 val[kVec];
+#pragma unroll
+      for (int u = 0; u < kVec; ++u)
+        if (v0 + 32 * u < nvec) val[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-          float s[8];
+          uint4 *dst = g + (int64_t)rows[j] * nvec;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) s[i] = wts[j] * f[i];
-          g[(int64_t)rows[j] * nvec + v] = pack8(s);
+          for (int u = 0; u < kVec; ++u) {
+            if (v0 + 32 * u < nvec) {
+              float f[8], sc[8];
+              unpack8(val[u], f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) sc[i] = wts[j] * f[i];
+              dst[v0 + 32 * u] = pack8(sc);
+            }
+          }
         }
       }
     }
@@ -381,11 +402,11 @@ cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *r
   if (C == 0) return cudaSuccess;
   if (with_count) {
     launch_begin(st);
-    route_kernel<true><<<C, 256, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+    route_kernel<true><<<C, 1024, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
     return note_launch("route_count", st);
   }
   launch_begin(st);
-  route_kernel<false><<<C, 256, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+  route_kernel<false><<<C, 1024, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
   return note_launch("route", st);
 }
 
