@@ -208,6 +208,17 @@ moe_status moe_dispatch_noalloc(moe_shape s, const moe_bf16 *x, const int32_t *i
                                 int32_t *counts, int32_t *offsets, int32_t *padded_offsets,
                                 int32_t *row_of, int32_t *tok_of, moe_stream stream);
 
+/* Failure test of the GEMM pipeline (no counterpart on the pages): runs the planning
+ * kernel and the gate_up GEMM of moe_expert_ffn with the TMA loads of every CTA's first
+ * k-block withheld, so that stage is never filled and every pipeline wait of the kernel
+ * gives up after wait_limit_us microseconds (1 .. 10^6). The kernel then records
+ * MOE_ERR_TIMEOUT in the status word of ws, waits (bounded) for its own copies, frees
+ * its tensor memory and returns; moe_check_device_status(ws) reports it and the CUDA
+ * context stays usable. h receives undefined values. Arguments as moe_expert_ffn. */
+moe_status moe_debug_gate_up_withheld(moe_shape s, const moe_bf16 *xp, const int32_t *counts,
+                                      const moe_bf16 *w_gu, moe_bf16 *h, void *ws,
+                                      size_t ws_bytes, int wait_limit_us, moe_stream stream);
+
 /* Device-side status of a workspace or scratch: synchronises `stream`, reads the
  * status word that the kernels set when a pipeline wait runs past its time limit,
  * and clears it. Returns MOE_OK or MOE_ERR_TIMEOUT. */

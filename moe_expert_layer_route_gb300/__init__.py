@@ -62,6 +62,8 @@ _SIG = {
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
                                     _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_check_device_status": (ctypes.c_int, [_c_vp, _c_vp]),
+    "moe_debug_gate_up_withheld": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                                  ctypes.c_size_t, ctypes.c_int, _c_vp]),
     "moe_profile_start": (ctypes.c_int, [ctypes.c_int]),
     "moe_profile_stop": (ctypes.c_int, [ctypes.POINTER(_LaunchTime), ctypes.c_int]),
     "moe_launch_count": (_c_i64, []),
@@ -309,6 +311,15 @@ def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Te
     return dx, dw_gu, dw_down
 
 
+def debug_gate_up_withheld(s: MoEShape, xp: torch.Tensor, counts: torch.Tensor,
+                           w_gu: torch.Tensor, ws: torch.Tensor, wait_limit_us: int) -> None:
+    """moe_debug_gate_up_withheld: the gate_up GEMM with its first loads withheld."""
+    h = torch.empty((padded_rows(s), s.f), dtype=torch.bfloat16, device=xp.device)
+    _check(lib().moe_debug_gate_up_withheld(s, _p(xp), _p(counts), _p(w_gu), _p(h), _p(ws),
+                                            ws.numel(), int(wait_limit_us), _stream()),
+           "moe_debug_gate_up_withheld")
+
+
 def check_device_status(ws_or_scratch: torch.Tensor) -> None:
     _check(lib().moe_check_device_status(_p(ws_or_scratch), _stream()), "moe_check_device_status")
 
@@ -332,5 +343,5 @@ def launch_count() -> int:
 
 __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
-           "dispatch", "dispatch_noalloc", "expert_ffn", "combine", "forward", "backward", "check_device_status",
+           "dispatch", "dispatch_noalloc", "expert_ffn", "combine", "forward", "backward", "check_device_status", "debug_gate_up_withheld",
            "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

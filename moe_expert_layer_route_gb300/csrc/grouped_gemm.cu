@@ -80,6 +80,9 @@ struct Args {
   const void *aux;  // DGRAD_H: GU
   int64_t ld_aux;
   int *status;
+  unsigned long long wait_ns;  // limit of every pipeline wait
+  int withhold_kblock;         // failure test only: the producer's k-block whose loads
+                               // are withheld (its stage never fills); -1 otherwise
 };
 
 // One CTA's share of a (pair-)tile: its 128 rows start at m0; valid is false when a
@@ -466,14 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = unit0; tile < total && ok; tile += units) {
         const Tile t = decode<KIND, PAIR>(a, tile, rank);
         for (int kb = 0; kb < t.kt; ++kb) {
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, a.status)) {
+          if (!mbar_wait(&empty_bar[s], ph ^ 1, a.status, a.wait_ns)) {
             ok = false;
             break;
           }
           uint8_t *sA = smem + s * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], (kPair ? 2 : 1) * kStageBytes);
           const uint32_t bar_pair = kPair ? mapa_shared(&full_bar[s], 0) : 0;
-          issue_loads<KIND, PAIR>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], bar_pair, t, kb, rank);
+          if (issued != a.withhold_kblock)
+            issue_loads<KIND, PAIR>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], bar_pair, t, kb,
+                                    rank);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -510,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t smem_base = smem_u32(smem);
       for (int tile = unit0; tile < total && ok; tile += units) {
         const Tile t = decode<KIND, PAIR>(a, tile, 0);
-        if (!mbar_wait(&acce_bar[buf], aph ^ 1, a.status)) {
+        if (!mbar_wait(&acce_bar[buf], aph ^ 1, a.status, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -522,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kPair) mbar_arrive_cluster(mapa_shared(&accf_bar[buf], 1));
         } else {
           for (int kb = 0; kb < t.kt; ++kb) {
-            if (!mbar_wait(&full_bar[s], ph, a.status)) {
+            if (!mbar_wait(&full_bar[s], ph, a.status, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = unit0; tile < total; tile += units) {
       const Tile t = decode<KIND, PAIR>(a, tile, rank);
       if (KIND == DGRAD_H && t.valid) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
-      bool ok = mbar_wait(&accf_bar[buf], aph, a.status);
+      bool ok = mbar_wait(&accf_bar[buf], aph, a.status, a.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         failed = true;
@@ -715,6 +720,8 @@ Args base_args(const GemmPlan &p, int *status) {
   a.E = p.E;
   a.status = status;
   a.weight_stationary = p.rows_per_expert <= kWeightStationaryMaxRows;
+  a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+  a.withhold_kblock = p.withhold_kblock;
   return a;
 }
 

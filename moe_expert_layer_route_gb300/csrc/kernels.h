@@ -63,6 +63,8 @@ struct GemmPlan {
   int E;
   int64_t R;                   // rows of the padded space
   int64_t rows_per_expert;     // T*k / E, the mean segment length (picks the tile order)
+  unsigned long long wait_ns = 0;  // pipeline wait limit (0 = the default kWaitLimitNs)
+  int withhold_kblock = -1;        // failure test: k-block whose loads are withheld
 };
 
 cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, void *h, void *gu,

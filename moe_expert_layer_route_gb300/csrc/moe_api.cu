@@ -347,6 +347,29 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   return MOE_OK;
 }
 
+moe_status moe_debug_gate_up_withheld(moe_shape s, const moe_bf16 *xp, const int32_t *counts,
+                                      const moe_bf16 *w_gu, moe_bf16 *h, void *ws,
+                                      size_t ws_bytes, int wait_limit_us, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(xp, counts, w_gu, h, ws));
+  if (wait_limit_us <= 0 || wait_limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int *status = at<int>(ws, L.status);
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
+  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
+  MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
+                       st));
+  GemmPlan p{padded, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
+  p.wait_ns = 1000ull * (unsigned long long)wait_limit_us;
+  p.withhold_kblock = 0;
+  MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, nullptr, (int)s.d, (int)s.f, status, st));
+  return MOE_OK;
+}
+
 moe_status moe_check_device_status(const void *ws_or_scratch, moe_stream stream) {
   if (!ws_or_scratch) return MOE_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
