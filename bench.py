@@ -184,18 +184,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- CPU oracle
 def oracle_step(oracle, inp_np: dict, n_tok: int, k: int) -> float:
-    """Forward + backward of the oracle on the first n_tok tokens; returns seconds."""
+    """Forward (+ backward when the workload has one) of the oracle on the first n_tok
+    tokens; returns seconds."""
     t0 = time.perf_counter()
     ref = oracle.forward(inp_np["x"][:n_tok], inp_np["logits"][:n_tok], inp_np["w_gu"],
                          inp_np["w_down"], k)
-    oracle.backward(inp_np["dy"][:n_tok], ref, inp_np["w_gu"], inp_np["w_down"])
+    if inp_np["dy"] is not None:
+        oracle.backward(inp_np["dy"][:n_tok], ref, inp_np["w_gu"], inp_np["w_down"])
     return time.perf_counter() - t0
 
 
-def oracle_inputs(inp: workloads.Inputs) -> dict:
+def oracle_inputs(inp: workloads.Inputs, backward: bool) -> dict:
     return {"x": inp.x.float().numpy(), "logits": inp.logits.numpy(),
             "w_gu": inp.w_gu.float().numpy(), "w_down": inp.w_down.float().numpy(),
-            "dy": inp.dy.float().numpy()}
+            "dy": inp.dy.float().numpy() if backward else None}
 
 
 def cpu_threads() -> int:
@@ -212,15 +214,16 @@ def cpu_threads() -> int:
 def cpu_baseline(wl, inp, seconds: float) -> dict:
     """The oracle as it stands on a bounded token sample sized to about `seconds`."""
     import oracle
-    inp_np = oracle_inputs(inp)
+    inp_np = oracle_inputs(inp, wl.backward)
     n = 16
     t = oracle_step(oracle, inp_np, n, wl.k)
     while t < seconds / 4 and n < wl.T:
         n = min(wl.T, n * 4)
         t = oracle_step(oracle, inp_np, n, wl.k)
     return {"value": n / t, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"first {n} of {wl.T} tokens of the {wl.name} workload, forward+backward "
-                      f"in fp64 numpy, {t:.1f} s"}
+            "sample": f"first {n} of {wl.T} tokens of the {wl.name} workload, "
+                      f"{'forward+backward' if wl.backward else 'forward'} in fp64 numpy, "
+                      f"{t:.1f} s"}
 
 
 # ---------------------------------------------------------------------- our arm
@@ -251,15 +254,16 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     x, logits = inp.x.to(dev), inp.logits.to(dev)
     w_gu, w_down, dy = inp.w_gu.to(dev), inp.w_down.to(dev), inp.dy.to(dev)
     s = moe.shape(wl.T, wl.d, wl.E, wl.k, wl.f)
-    ws = moe.new_workspace(s, True, dev)
+    ws = moe.new_workspace(s, wl.backward, dev)
     scratch = moe.new_scratch(s, dev)
     y = torch.empty_like(x)
     grads = (torch.empty_like(x), torch.empty_like(w_gu), torch.empty_like(w_down))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        moe.forward(x, logits, w_gu, w_down, wl.k, training=True, ws=ws, y=y)
-        moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads)
+        moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y)
+        if wl.backward:
+            moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads)
 
     for _ in range(args.warmup):
         step()
@@ -354,10 +358,12 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         def e2e_step():
             x.copy_(hx, non_blocking=True)
             logits.copy_(hl, non_blocking=True)
-            dy.copy_(hdy, non_blocking=True)
+            if wl.backward:
+                dy.copy_(hdy, non_blocking=True)
             step()
             hy.copy_(y, non_blocking=True)
-            hdx.copy_(grads[0], non_blocking=True)
+            if wl.backward:
+                hdx.copy_(grads[0], non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -373,8 +379,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) * 1e3 / ke
         e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
-        h2d = hx.numel() * 2 + hl.numel() * 4 + hdy.numel() * 2
-        d2h = hy.numel() * 2 + hdx.numel() * 2
+        h2d = hx.numel() * 2 + hl.numel() * 4 + (hdy.numel() * 2 if wl.backward else 0)
+        d2h = hy.numel() * 2 + (hdx.numel() * 2 if wl.backward else 0)
         e2e = {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
@@ -385,10 +391,11 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
-                   "f": wl.f, "seed": wl.seed, "passes": "forward+backward",
+                   "f": wl.f, "seed": wl.seed,
+                   "passes": "forward+backward" if wl.backward else "forward",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed (256 MB write) before each timed step, outside its events; "
-                         "weights alone are 2.1 GB"},
+                         f"weights alone are {6 * wl.E * wl.d * wl.f / 1e9:.2f} GB"},
         "gemm_tflops": gemm_tflops,
         "gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16_tflops_sustained"],
         "gemm_flop_per_step": gemm_flop,
@@ -410,8 +417,8 @@ def run_reference(args, rank, world) -> dict | None:
         return None
     import oracle
     wl = workload_of(args)
-    inp = workloads.make_inputs(wl, with_dy=True)
-    inp_np = oracle_inputs(inp)
+    inp = workloads.make_inputs(wl, with_dy=wl.backward)
+    inp_np = oracle_inputs(inp, wl.backward)
     budget = args.reference_seconds / max(1, args.steps + args.warmup)
     n = 4
     t = oracle_step(oracle, inp_np, n, wl.k)
@@ -425,14 +432,15 @@ def run_reference(args, rank, world) -> dict | None:
     value = n / sec
     cores = cpu_threads()
     sample = (f"first {n} of {wl.T} tokens of the {wl.name} workload per step, "
-              f"forward+backward in fp64 numpy")
+              f"{'forward+backward' if wl.backward else 'forward'} in fp64 numpy")
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
-                   "f": wl.f, "seed": wl.seed, "passes": "forward+backward"},
+                   "f": wl.f, "seed": wl.seed,
+                   "passes": "forward+backward" if wl.backward else "forward"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
