@@ -31,7 +31,9 @@ What the method computes, and where it is stated:
 * Backward -- "Halo: Frontier-Lab Training for Everyone", section "The hard
   problems along the way" (atomic-free routing backward) and the LoRA paragraph
   of "One trainer architecture" (expert gradients). Gradients of Y with respect
-  to x, W_gu and W_down, routing weights held constant.
+  to x, W_gu and W_down with the routing weights held constant, and (router_backward)
+  the gradient with respect to the router logits through the routing weights, the
+  top-k selection held fixed.
 """
 from __future__ import annotations
 
@@ -239,6 +241,39 @@ def backward(dy, fwd: dict, w_gu, w_down) -> dict:
     for j in range(k):
         dX += dXp[row_of[:, j]]
     return {"g": G, "dgu": dGU, "dxp": dXp, "dx": dX, "dw_gu": dW_gu, "dw_down": dW_down}
+
+
+def router_backward(dy, fwd: dict) -> np.ndarray:
+    """Gradient of the loss <dY, Y> with respect to the router logits.
+
+    "The hard problems along the way" ("Halo: Frontier-Lab Training for Everyone")
+    credits a routing backward without atomics. Y[t] = sum_j w[t, j] O[row_of[t, j]]
+    with w the softmax over the k chosen logits, so with dw_j = <dY[t], O[row_of[t, j]]>
+    the chain rule through that softmax gives, for the chosen experts,
+    dlogit[t, ids[t, j]] = w_j * (dw_j - sum_i w_i dw_i); the others get 0 (the
+    selection itself is piecewise constant). Returns [T, E] float64.
+    """
+    dy = np.asarray(dy, dtype=F64)
+    T = dy.shape[0]
+    ids, w, row_of, o = fwd["ids"], fwd["w"], fwd["row_of"], fwd["o"]
+    E = int(fwd["counts"].shape[0])
+    dw = np.einsum("td,tjd->tj", dy, np.asarray(o, dtype=F64)[row_of])
+    centred = dw - (w * dw).sum(axis=1, keepdims=True)
+    dl = np.zeros((T, E), dtype=F64)
+    np.put_along_axis(dl, np.asarray(ids, dtype=np.int64), w * centred, axis=1)
+    return dl
+
+
+def router_backward_token(x_t, dy_t, ids_t, w_t, E: int, w_gu, w_down) -> np.ndarray:
+    """dlogit[t, :] for one token from its own routing (one-at-a-time form)."""
+    x_t = np.asarray(x_t, dtype=F64)
+    dy_t = np.asarray(dy_t, dtype=F64)
+    dw = np.array([dy_t @ swiglu_expert(x_t[None, :], w_gu[int(e)], w_down[int(e)])["o"][0]
+                   for e in ids_t])
+    w_t = np.asarray(w_t, dtype=F64)
+    dl = np.zeros(E, dtype=F64)
+    dl[np.asarray(ids_t, dtype=np.int64)] = w_t * (dw - (w_t * dw).sum())
+    return dl
 
 
 # ------------------------------------------------------- single outputs, one at a time

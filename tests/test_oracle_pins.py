@@ -258,6 +258,36 @@ def test_backward_directional_derivative():
     assert abs(fd - an) <= 1e-7 * max(1.0, abs(fd))
 
 
+def test_router_backward_matches_finite_differences():
+    """d<dY, Y>/d logits by central differences. The logits are multiples of 2^-6 and
+    the step is 2^-12, so every perturbed fp32 logit is exact and no top-k choice
+    changes (the gaps between distinct logits are at least 2^-6)."""
+    x, _, w_gu, w_down, dy, k = _tiny(T=6, d=12, E=5, k=3, f=10, seed=17)
+    rng = np.random.default_rng(18)
+    logits = (rng.integers(-128, 128, size=(6, 5)) / 64.0).astype(np.float32)
+    out = oracle.forward(x, logits, w_gu, w_down, k)
+    dl = oracle.router_backward(dy, out)
+    h = 2.0 ** -12
+    for t in range(6):
+        for e in range(5):
+            lp, lm = logits.copy(), logits.copy()
+            lp[t, e] += np.float32(h)
+            lm[t, e] -= np.float32(h)
+            fd = (_loss(x, lp, w_gu, w_down, k, dy) - _loss(x, lm, w_gu, w_down, k, dy)) / (2 * h)
+            assert abs(fd - dl[t, e]) <= 1e-6 * max(1.0, abs(fd)), (t, e, fd, dl[t, e])
+    chosen = np.zeros_like(dl, dtype=bool)
+    np.put_along_axis(chosen, out["ids"].astype(np.int64), True, axis=1)
+    assert not dl[~chosen].any()
+    np.testing.assert_allclose(dl.sum(axis=1), 0.0, atol=1e-12)   # softmax Jacobian rows sum to 0
+
+
+def test_router_backward_k1_is_zero():
+    """With one expert per token the weight is 1 whatever the logit: no gradient."""
+    x, logits, w_gu, w_down, dy, _ = _tiny(T=9, d=8, E=4, k=1, f=8, seed=19)
+    out = oracle.forward(x, logits, w_gu, w_down, 1)
+    assert not oracle.router_backward(dy, out).any()
+
+
 # ----------------------------------------------- one-at-a-time outputs vs the full oracle
 def test_single_output_helpers_agree_with_full_oracle():
     x, logits, w_gu, w_down, dy, k = _tiny(T=30, d=16, E=5, k=2, f=12, seed=16)
@@ -270,6 +300,9 @@ def test_single_output_helpers_agree_with_full_oracle():
         np.testing.assert_allclose(
             oracle.backward_token(x[t], dy[t], out["ids"][t], out["w"][t], w_gu, w_down),
             g["dx"][t], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(
+            oracle.router_backward_token(x[t], dy[t], out["ids"][t], out["w"][t], 5, w_gu, w_down),
+            oracle.router_backward(dy, out)[t], rtol=1e-12, atol=1e-15)
     for e in range(5):
         rows = np.array([0, 3, 11])
         np.testing.assert_allclose(
@@ -315,8 +348,16 @@ def _bwd_missing_term(dh, g, u):
     return dh * u * s, dh * g * s                               # drops (1 + g(1 - s))
 
 
+def _router_bwd_uncentred(dy, fwd):
+    dy = np.asarray(dy, dtype=np.float64)
+    dw = np.einsum("td,tjd->tj", dy, np.asarray(fwd["o"], dtype=np.float64)[fwd["row_of"]])
+    dl = np.zeros((dy.shape[0], int(fwd["counts"].shape[0])))
+    np.put_along_axis(dl, fwd["ids"].astype(np.int64), fwd["w"] * dw, axis=1)  # no centring
+    return dl
+
+
 @pytest.mark.parametrize("mutant", ["swapped_gate_up", "reversed_down_rows", "ties_high",
-                                    "bwd_missing_term"])
+                                    "bwd_missing_term", "router_uncentred"])
 def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     caught = False
     if mutant == "swapped_gate_up":
@@ -342,6 +383,12 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
         monkeypatch.setattr(moe_oracle, "swiglu_backward", _bwd_missing_term)
         try:
             test_backward_matches_central_finite_differences()
+        except AssertionError:
+            caught = True
+    elif mutant == "router_uncentred":
+        monkeypatch.setattr(oracle, "router_backward", _router_bwd_uncentred)
+        try:
+            test_router_backward_matches_finite_differences()
         except AssertionError:
             caught = True
     assert caught, f"no pin caught the planted mistake {mutant}"
