@@ -120,6 +120,7 @@ def kernel_work(wl: workloads.Workload) -> dict:
         "scatter": ("byte", T * d * 2 + A * d * 2 + A * 16),
         "combine": ("byte", A * d * 2 + A * 8 + T * d * 2),
         "g_scatter": ("byte", T * d * 2 + A * d * 2 + A * 8),
+        "g_scatter_router_grad": ("byte", T * d * 2 + 2 * A * d * 2 + A * 12 + T * E * 4),
         "dx_gather": ("byte", A * d * 2 + A * 4 + T * d * 2),
     }
 
@@ -258,12 +259,13 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     scratch = moe.new_scratch(s, dev)
     y = torch.empty_like(x)
     grads = (torch.empty_like(x), torch.empty_like(w_gu), torch.empty_like(w_down))
+    dlogits = torch.empty_like(logits) if args.router_grad else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
         moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y)
         if wl.backward:
-            moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads)
+            moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads, dlogits=dlogits)
 
     for _ in range(args.warmup):
         step()
@@ -392,7 +394,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                    "f": wl.f, "seed": wl.seed,
-                   "passes": "forward+backward" if wl.backward else "forward",
+                   "passes": ("forward+backward" if wl.backward else "forward")
+                   + (" + router-logit gradient" if args.router_grad and wl.backward else ""),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed (256 MB write) before each timed step, outside its events; "
                          f"weights alone are {6 * wl.E * wl.d * wl.f / 1e9:.2f} GB"},
@@ -458,6 +461,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
+    ap.add_argument("--router-grad", action="store_true",
+                    help="also compute the router-logit gradient in the backward")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (profiling a smaller case; not a headline line)")
     ap.add_argument("--experts", type=int, default=None,

@@ -170,22 +170,26 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
                        const moe_bf16 *w_down, moe_bf16 *y, int training, void *ws,
                        size_t ws_bytes, moe_stream stream);
 
-/* Backward of the block for dY, the routing weights held constant ("Halo: Frontier-Lab
- * Training for Everyone", "The hard problems along the way": an atomic-free routing
- * backward). With G[r] = w[t][j] * dY[t] for r = row_of[t][j]:
+/* Backward of the block for dY ("Halo: Frontier-Lab Training for Everyone", "The hard
+ * problems along the way": an atomic-free routing backward). With
+ * G[r] = w[t][j] * dY[t] for r = row_of[t][j]:
  *   dW_down[e] = H_e^T G_e;  dH = G W_down[e]^T;  dgate = dH * up * silu'(gate),
  *   dup = dH * silu(gate);   dW_gu[e] = Xp_e^T [dgate | dup];
- *   dXp = [dgate | dup] W_gu[e]^T;  dX[t] = sum_j dXp[row_of[t][j]] (a gather).
+ *   dXp = [dgate | dup] W_gu[e]^T;  dX[t] = sum_j dXp[row_of[t][j]] (a gather);
+ * and, when dlogits is not NULL, the router-logit gradient through the routing
+ * weights (the top-k choice held fixed): with dw_j = <dY[t], O[row_of[t][j]]>,
+ *   dlogits[t][ids[t][j]] = w_j * (dw_j - sum_i w_i dw_i), 0 for the other experts.
  * Every gradient is written by exactly one thread (no atomics, bit-reproducible);
  * experts with no rows get dW = 0.
  *   dy [T x d] bf16 in; w_gu, w_down as in moe_forward; ws: the workspace of a
  *   moe_forward(training = 1) call with the same shape and weights;
  *   dx [T x d], dw_gu [E x d x 2f], dw_down [E x f x d] bf16 out;
+ *   dlogits [T x E] fp32 out or NULL;
  *   scratch: at least moe_backward_scratch_size(s) bytes. */
 moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
                         const moe_bf16 *w_down, const void *ws, size_t ws_bytes, moe_bf16 *dx,
-                        moe_bf16 *dw_gu, moe_bf16 *dw_down, void *scratch, size_t scratch_bytes,
-                        moe_stream stream);
+                        moe_bf16 *dw_gu, moe_bf16 *dw_down, float *dlogits, void *scratch,
+                        size_t scratch_bytes, moe_stream stream);
 
 /* Dispatch without a workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart of this call: it exists for callers that have no

@@ -60,7 +60,7 @@ _SIG = {
     "moe_forward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_int,
                                    _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
-                                    _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+                                    _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_check_device_status": (ctypes.c_int, [_c_vp, _c_vp]),
     "moe_debug_gate_up_withheld": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                                   ctypes.c_size_t, ctypes.c_int, _c_vp]),
@@ -293,8 +293,10 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w_gu: torch.Tensor, w_down: t
 
 def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Tensor,
              ws: torch.Tensor, scratch: torch.Tensor | None = None,
-             out: tuple | None = None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """moe_backward: (dx, dw_gu, dw_down) for the forward that filled ws (training=True)."""
+             out: tuple | None = None, router_grad: bool = False,
+             dlogits: torch.Tensor | None = None):
+    """moe_backward: (dx, dw_gu, dw_down) for the forward that filled ws (training=True),
+    plus dlogits [T, E] fp32 as a fourth element when router_grad (or dlogits) is given."""
     _want(dy, torch.bfloat16, "dy")
     dev = dy.device
     if scratch is None:
@@ -305,9 +307,16 @@ def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Te
         dw_down = torch.empty(tuple(w_down.shape), dtype=torch.bfloat16, device=dev)
     else:
         dx, dw_gu, dw_down = out
+    if router_grad and dlogits is None:
+        dlogits = torch.empty((s.T, s.E), dtype=torch.float32, device=dev)
+    if dlogits is not None:
+        _want(dlogits, torch.float32, "dlogits")
     _check(lib().moe_backward(s, _p(dy), _p(w_gu), _p(w_down), _p(ws), ws.numel(), _p(dx),
-                              _p(dw_gu), _p(dw_down), _p(scratch), scratch.numel(), _stream()),
+                              _p(dw_gu), _p(dw_down), _p(dlogits), _p(scratch), scratch.numel(),
+                              _stream()),
            "moe_backward")
+    if dlogits is not None:
+        return dx, dw_gu, dw_down, dlogits
     return dx, dw_gu, dw_down
 
 

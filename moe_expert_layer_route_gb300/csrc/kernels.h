@@ -37,9 +37,11 @@ cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of,
                            int d, int k, cudaStream_t st);
 cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, int T, int d,
                               int k, cudaStream_t st);
+// with dlogits (T x E fp32, may be null) also the router-logit gradient from o and ids
 cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *row_of,
                                  const int32_t *padded, const int32_t *counts, void *g, int T,
-                                 int d, int E, int k, cudaStream_t st);
+                                 int d, int E, int k, const void *o, const int32_t *ids,
+                                 float *dlogits, cudaStream_t st);
 
 // grouped_gemm.cu -- the tcgen05 grouped GEMM engine.
 //

@@ -316,11 +316,12 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
 
 moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
                         const moe_bf16 *w_down, const void *ws, size_t ws_bytes, moe_bf16 *dx,
-                        moe_bf16 *dw_gu, moe_bf16 *dw_down, void *scratch, size_t scratch_bytes,
-                        moe_stream stream) {
+                        moe_bf16 *dw_gu, moe_bf16 *dw_down, float *dlogits, void *scratch,
+                        size_t scratch_bytes, moe_stream stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(check_ptrs(w_gu, w_down, ws, dw_gu, dw_down, scratch));
   if (s.T > 0) MOE_TRY(check_ptrs(dy, dx));
+  if (dlogits && !aligned16(dlogits)) return MOE_ERR_ALIGNMENT;
   const FwdLayout L = fwd_layout(s, 1);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   const BwdLayout B = bwd_layout(s);
@@ -334,11 +335,14 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   const int32_t *padded = at<int32_t>(fws, L.padded), *tiles = at<int32_t>(fws, L.tile_expert);
   const int32_t *pstart = at<int32_t>(fws, L.pair_start), *pexp = at<int32_t>(fws, L.pair_expert);
   const void *xp = at<void>(fws, L.xp), *gu = at<void>(fws, L.gu), *h = at<void>(fws, L.h);
+  const void *o = at<void>(fws, L.o);
+  const int32_t *ids = at<int32_t>(fws, L.ids);
   int *status = at<int>(scratch, B.status);
   void *g = at<void>(scratch, B.g), *dgu = at<void>(scratch, B.dgu), *dxp = at<void>(scratch, B.dxp);
   const GemmPlan p{padded, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
-  MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, st));
+  MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, o, ids,
+                                s.T > 0 ? dlogits : nullptr, st));
   MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));
   MOE_CUDA(gemm_wgrad(p, h, g, dw_down, f, d, status, "gemm_wgrad_down", st));
   MOE_CUDA(gemm_dgrad_x(p, dgu, w_gu, dxp, d, f, status, st));

@@ -340,10 +340,18 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict
 // ------------------------------------------------------------------ backward scatter
 // G[row_of[t][j]] = bf16(w[t][j] * dY[t]) (one warp per token); the extra E blocks
 // zero each expert's padding rows of G so the GEMMs read zeros there.
+//
+// With dlogits, the same pass also forms the router-logit gradient of the token
+// ("The hard problems along the way" in "Halo: Frontier-Lab Training for Everyone":
+// a routing backward without atomics): dw_j = <dY[t], O[row_of[t][j]]> in fp32 (each
+// lane's partial sums, then a fixed-order warp reduction), then
+// dlogits[t][ids[t][j]] = w_j (dw_j - sum_i w_i dw_i) and 0 for the other experts. The
+// whole row of each token is written by its warp.
 __global__ void __launch_bounds__(256) scale_scatter_kernel(
     const uint4 *__restrict__ dy, const float *__restrict__ w, const int32_t *__restrict__ row_of,
     const int32_t *__restrict__ padded, const int32_t *__restrict__ counts,
-    uint4 *__restrict__ g, int T, int nvec, int E, int k, int token_blocks) {
+    uint4 *__restrict__ g, int T, int nvec, int E, int k, int token_blocks,
+    const uint4 *__restrict__ o, const int32_t *__restrict__ ids, float *__restrict__ dlogits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x < token_blocks) {
     const int t = blockIdx.x * 8 + warp;
@@ -355,18 +363,43 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
       wt = w[(int64_t)t * k + lane];
     }
     int rows[kMaxK];
-    float wts[kMaxK];
+    float wts[kMaxK], dot[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       rows[j] = __shfl_sync(0xffffffffu, row, j);
       wts[j] = __shfl_sync(0xffffffffu, wt, j);
+      dot[j] = 0.f;
     }
+    const bool router = dlogits != nullptr;
     const uint4 *src = dy + (int64_t)t * nvec;
     for (int v0 = lane; v0 < nvec; v0 += 32 * kVec) {
       uint4 val[kVec];
 #pragma unroll
       for (int u = 0; u < kVec; ++u)
         if (v0 + 32 * u < nvec) val[u] = __ldg(src + v0 + 32 * u);
+      if (router) {
+        // the dot products first: kVec output-row loads in flight per slot
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j < k) {
+            const uint4 *orow = o + (int64_t)rows[j] * nvec;
+            uint4 ov[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u)
+              if (v0 + 32 * u < nvec) ov[u] = __ldg(orow + v0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+              if (v0 + 32 * u < nvec) {
+                float f[8], of[8];
+                unpack8(val[u], f);
+                unpack8(ov[u], of);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot[j] = fmaf(f[i], of[i], dot[j]);
+              }
+            }
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
@@ -382,6 +415,26 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
             }
           }
         }
+      }
+    }
+    if (router) {
+      float s = 0.f;
+      int eid[kMaxK];
+      const int my_id = (lane < k) ? ids[(int64_t)t * k + lane] : -1;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], off);
+        eid[j] = __shfl_sync(0xffffffffu, my_id, j);
+        if (j < k) s = fmaf(wts[j], dot[j], s);
+      }
+      float *out = dlogits + (int64_t)t * E;
+      for (int e = lane; e < E; e += 32) {
+        float val = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+          if (j < k && eid[j] == e) val = wts[j] * (dot[j] - s);
+        out[e] = val;
       }
     }
   } else {
@@ -471,13 +524,14 @@ cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, 
 
 cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *row_of,
                                  const int32_t *padded, const int32_t *counts, void *g, int T,
-                                 int d, int E, int k, cudaStream_t st) {
+                                 int d, int E, int k, const void *o, const int32_t *ids,
+                                 float *dlogits, cudaStream_t st) {
   const int token_blocks = ceil_div(T, 8);
   launch_begin(st);
-  scale_scatter_kernel<<<token_blocks + E, 256, 0, st>>>((const uint4 *)dy, w, row_of, padded,
-                                                         counts, (uint4 *)g, T, d / 8, E, k,
-                                                         token_blocks);
-  return note_launch("g_scatter", st);
+  scale_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(
+      (const uint4 *)dy, w, row_of, padded, counts, (uint4 *)g, T, d / 8, E, k, token_blocks,
+      (const uint4 *)o, ids, dlogits);
+  return note_launch(dlogits ? "g_scatter_router_grad" : "g_scatter", st);
 }
 
 }  // namespace moe

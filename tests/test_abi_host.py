@@ -93,10 +93,12 @@ def test_pointer_and_workspace_validation(moe):
     assert L.moe_forward(s, odd, good, good, good, good, 1, good, need, None) == -3
     assert L.moe_forward(s, good, good, good, good, good, 1, good, need - 1, None) == -4
     scratch = L.moe_backward_scratch_size(s)
-    assert L.moe_backward(s, good, good, good, good, need, good, good, good, good, scratch - 1,
-                          None) == -4
-    assert L.moe_backward(s, good, good, good, good, need - 1, good, good, good, good, scratch,
-                          None) == -4
+    assert L.moe_backward(s, good, good, good, good, need, good, good, good, null, good,
+                          scratch - 1, None) == -4
+    assert L.moe_backward(s, good, good, good, good, need - 1, good, good, good, null, good,
+                          scratch, None) == -4
+    assert L.moe_backward(s, good, good, good, good, need, good, good, good, odd, good,
+                          scratch, None) == -3
     assert L.moe_combine(s, good, good, good, null, None) == -1
     assert L.moe_route(s, good, good, odd, None) == -3
 

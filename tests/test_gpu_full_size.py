@@ -32,7 +32,8 @@ def test_workload_full_size(moe, name):
     y, ws, s = moe.forward(inp.x.to(dev), inp.logits.to(dev), w_gu, w_down, wl.k,
                            training=wl.backward)
     if wl.backward:
-        dx, dw_gu, dw_down = moe.backward(s, inp.dy.to(dev), w_gu, w_down, ws)
+        dx, dw_gu, dw_down, dl = moe.backward(s, inp.dy.to(dev), w_gu, w_down, ws,
+                                              router_grad=True)
     torch.cuda.synchronize()
     moe.check_device_status(ws)
 
@@ -70,6 +71,9 @@ def test_workload_full_size(moe, name):
     dx_ref = np.stack([oracle.backward_token(x64[i], dy64[i], rid[t], rw[t], WG, WD)
                        for i, t in enumerate(toks)])
     assert_close(to_np(dx[torch.from_numpy(toks).to(dev)]), dx_ref, "dX (sampled tokens)")
+    dl_ref = np.stack([oracle.router_backward_token(x64[i], dy64[i], rid[t], rw[t], wl.E, WG, WD)
+                       for i, t in enumerate(toks)])
+    assert_close(to_np(dl[torch.from_numpy(toks).to(dev)]), dl_ref, "dlogits (sampled tokens)")
 
     counts = ref["counts"]
     experts = {int(np.argmax(counts)), int(np.argmin(counts)), int(rng.integers(wl.E))}

@@ -172,11 +172,17 @@ def test_backward_parity(moe, c):
     g = oracle.backward(DY, ref, Wg, Wd)
     w_gu, w_down = inp.w_gu.to(DEV), inp.w_down.to(DEV)
     y, ws, s = moe.forward(inp.x.to(DEV), inp.logits.to(DEV), w_gu, w_down, wl.k, training=True)
-    dx, dw_gu, dw_down = moe.backward(s, inp.dy.to(DEV), w_gu, w_down, ws)
+    dx, dw_gu, dw_down, dl = moe.backward(s, inp.dy.to(DEV), w_gu, w_down, ws, router_grad=True)
     torch.cuda.synchronize()
     moe.check_device_status(ws)
     assert_close(to_np(y), ref["y"], "Y")
     assert_close(to_np(dx), g["dx"], "dX")
+    dl_ref = oracle.router_backward(DY, ref)
+    if wl.k == 1:
+        assert not dl.any()                         # weight 1 whatever the logit
+    else:
+        assert_close(to_np(dl), dl_ref, "dlogits")
+    assert not to_np(dl)[dl_ref == 0].any()         # unchosen experts get exactly 0
     assert_close_experts(to_np(dw_gu), g["dw_gu"], "dW_gu")
     assert_close_experts(to_np(dw_down), g["dw_down"], "dW_down")
     empty = np.nonzero(ref["counts"] == 0)[0]
@@ -206,8 +212,9 @@ def test_determinism(moe):
     for _ in range(2):
         y, ws, s = moe.forward(inp.x.to(DEV), inp.logits.to(DEV), w_gu, w_down, wl.k,
                                training=True)
-        dx, dwg, dwd = moe.backward(s, inp.dy.to(DEV), w_gu, w_down, ws)
+        dx, dwg, dwd, dl = moe.backward(s, inp.dy.to(DEV), w_gu, w_down, ws, router_grad=True)
         v = moe.workspace_views(s, True, ws)
-        outs.append([t.clone() for t in (y, dx, dwg, dwd, v["ids"], v["row_of"], v["tok_of"])])
+        outs.append([t.clone() for t in (y, dx, dwg, dwd, dl, v["ids"], v["row_of"],
+                                          v["tok_of"])])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
