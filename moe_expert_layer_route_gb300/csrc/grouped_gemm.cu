@@ -65,6 +65,7 @@ enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
 
 struct Args {
   const int32_t *padded;       // [E+1]
+  const int32_t *counts;       // [E] rows of each expert (WGRAD: the K extent)
   const int32_t *tile_expert;  // [R/128]
   const int32_t *pair_start;   // [E+1] (pair mode)
   const int32_t *pair_expert;  // pair-tile -> expert (pair mode)
@@ -112,7 +113,7 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
     t.m0 = (r / a.n_tiles) * kMTile + rank * BM;
     t.n0 = (r % a.n_tiles) * BN;
     t.kr0 = a.padded[t.e];
-    t.kt = (a.padded[t.e + 1] - t.kr0) / BK;
+    t.kt = (a.counts[t.e] + BK - 1) / BK;  // k-blocks holding the expert's rows
     return t;
   }
   // ragged M: "units" are 128-row tiles (single) or pairs of them (pair mode);
@@ -230,7 +231,7 @@ struct Stager {
   }
 };
 
-__device__ __forceinline__ void put32(uint8_t *b, int lane, const float (&x)[32]) {
+__device__ __forceinline__ void put32(uint8_t *b, int lane, const float *x) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     float o[8];
@@ -240,70 +241,95 @@ __device__ __forceinline__ void put32(uint8_t *b, int lane, const float (&x)[32]
   }
 }
 
+// Write one 32 x 32 chunk of bf16 values (this lane's row: x[0..31]) through the next
+// staging buffer and a TMA store at coordinates c (clipped at the tensor's edges).
+template <int NC>
+__device__ __forceinline__ void emit_chunk(Stager &st, int lane, const float *x,
+                                           const CUtensorMap *tm, const int (&c)[NC]) {
+  uint8_t *b = st.next(lane);
+  put32(b, lane, x);
+  st.publish();
+  if (lane == 0) {
+    if (NC == 2) tma_store_2d(tm, b, c[0], c[1]);
+    else tma_store_3d(tm, b, c[0], c[1], c[NC - 1]);
+    bulk_commit();
+  }
+  ++st.n;
+}
+
+// Hand the accumulator buffer back to the MMA issuer (once this warp's TMEM reads are
+// complete).
+__device__ __forceinline__ void release_acc(int lane, uint64_t *bar_local, uint32_t bar_pair,
+                                            bool pair) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (pair) mbar_arrive_cluster(bar_pair);
+    else mbar_arrive(bar_local);
+  }
+}
+
 // Epilogue of one tile for one warp: TMEM lanes of quarter q (rows m0+32q ..), the
-// accumulator columns of half ch of the tile.
+// accumulator columns of half ch of the tile. Except for DGRAD_H, the warp reads all
+// its accumulator columns into registers first and releases the accumulator (rel_*)
+// before it converts and stores, so the next tile's MMAs need not wait for the stores.
+// Returns whether it released the accumulator.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Args &a, const Tile &t, uint32_t taddr,
+__device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint32_t taddr,
                                               int q, int ch, int lane, Stager &st,
-                                              const CUtensorMap *tmO, const CUtensorMap *tmO2) {
+                                              const CUtensorMap *tmO, const CUtensorMap *tmO2,
+                                              uint64_t *rel_local, uint32_t rel_pair,
+                                              bool pair) {
   const int row0 = t.m0 + 32 * q;  // first row of this warp's 32-row slab
   if (KIND == GATE_UP) {
     // accumulator columns [0,128) gate, [128,256) up; this warp: h columns ch*64 ..+63
-#pragma unroll 1
-    for (int c32 = ch * 64; c32 < ch * 64 + 64; c32 += 32) {
-      const int col = t.n0 + c32;
-      if (col >= a.f) break;
-      float g[32], u[32];
-      tmem_ld32x2(taddr + c32, taddr + BN / 2 + c32, g, u);
-      uint8_t *b = st.next(lane);
-      {
-        float h[32];
+    float g[64], u[64];
+    tmem_ld64x2(taddr + ch * 64, taddr + BN / 2 + ch * 64, g, u);
+    release_acc(lane, rel_local, rel_pair, pair);
+    if (!t.valid) return true;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) h[i] = silu(g[i]) * u[i];
-        put32(b, lane, h);
-      }
-      st.publish();
-      if (lane == 0) {
-        tma_store_2d(tmO, b, col, row0);
-        bulk_commit();
-      }
-      ++st.n;
-      if (a.out2) {
-        uint8_t *bg = st.next(lane);
-        put32(bg, lane, g);
-        st.publish();
-        if (lane == 0) {
-          tma_store_3d(tmO2, bg, col, 0, row0);
-          bulk_commit();
+    for (int c = 0; c < 2; ++c) {
+      const int col = t.n0 + ch * 64 + 32 * c;
+      if (col < a.f) {
+        if (a.out2) {  // the saved pre-activations first, then h in place over gate
+          const int cg[3] = {col, 0, row0}, cu[3] = {col, 1, row0};
+          emit_chunk<3>(st, lane, g + 32 * c, tmO2, cg);
+          emit_chunk<3>(st, lane, u + 32 * c, tmO2, cu);
         }
-        ++st.n;
-        uint8_t *bu = st.next(lane);
-        put32(bu, lane, u);
-        st.publish();
-        if (lane == 0) {
-          tma_store_3d(tmO2, bu, col, 1, row0);
-          bulk_commit();
-        }
-        ++st.n;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[32 * c + i] = silu(g[32 * c + i]) * u[32 * c + i];
+        const int ch2[2] = {col, row0};
+        emit_chunk<2>(st, lane, g + 32 * c, tmO, ch2);
       }
     }
-  } else if (KIND == DOWN || KIND == DGRAD_X) {
-#pragma unroll 1
-    for (int c32 = ch * 128; c32 < ch * 128 + 128; c32 += 32) {
-      const int col = t.n0 + c32;
-      if (col >= a.N_out) break;
-      float x[32];
-      tmem_ld32(taddr + c32, x);
-      uint8_t *b = st.next(lane);
-      put32(b, lane, x);
-      st.publish();
-      if (lane == 0) {
-        tma_store_2d(tmO, b, col, row0);
-        bulk_commit();
-      }
-      ++st.n;
+    return true;
+  } else if (KIND == DOWN || KIND == DGRAD_X || KIND == WGRAD) {
+    float x[128];
+    if (KIND == WGRAD && t.kt == 0) {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) x[i] = 0.f;
+    } else {
+      tmem_ld128(taddr + ch * 128, x);
     }
-  } else if (KIND == DGRAD_H) {
+    release_acc(lane, rel_local, rel_pair, pair);
+    if (!t.valid) return true;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int col = t.n0 + ch * 128 + 32 * c;
+      const bool ok = col < a.N_out && (KIND != WGRAD || row0 < a.M_out);
+      if (ok) {
+        if (KIND == WGRAD) {
+          const int cw[3] = {col, row0, t.e};
+          emit_chunk<3>(st, lane, x + 32 * c, tmO, cw);
+        } else {
+          const int co[2] = {col, row0};
+          emit_chunk<2>(st, lane, x + 32 * c, tmO, co);
+        }
+      }
+    }
+    return true;
+  } else {  // DGRAD_H
+    if (!t.valid) return false;
     // dH -> (dgate, dup) with the saved gate/up pre-activations of this row; the
     // gate/up values of the next 32 columns are loaded while these are computed.
     const int64_t row = row0 + lane;
@@ -359,27 +385,7 @@ __device__ __forceinline__ void epilogue_tile(const Args &a, const Tile &t, uint
         cu[v] = nu[v];
       }
     }
-  } else {  // WGRAD
-#pragma unroll 1
-    for (int c32 = ch * 128; c32 < ch * 128 + 128; c32 += 32) {
-      const int col = t.n0 + c32;
-      if (col >= a.N_out || row0 >= a.M_out) break;
-      float x[32];
-      if (t.kt > 0) {
-        tmem_ld32(taddr + c32, x);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = 0.f;
-      }
-      uint8_t *b = st.next(lane);
-      put32(b, lane, x);
-      st.publish();
-      if (lane == 0) {
-        tma_store_3d(tmO, b, col, row0, t.e);
-        bulk_commit();
-      }
-      ++st.n;
-    }
+    return false;
   }
 }
 
@@ -586,13 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
-      if (t.valid) epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (kPair) mbar_arrive_cluster(buf ? acce_pair1 : acce_pair0);
-        else mbar_arrive(&acce_bar[buf]);
-      }
+      const bool released =
+          epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2, &acce_bar[buf],
+                              buf ? acce_pair1 : acce_pair0, kPair);
+      if (!released) release_acc(lane, &acce_bar[buf], buf ? acce_pair1 : acce_pair0, kPair);
       buf ^= 1;
       if (buf == 0) aph ^= 1;
     }
@@ -714,6 +717,7 @@ cudaError_t launch_kind(bool pair, const CUtensorMap &tmA, const CUtensorMap &tm
 Args base_args(const GemmPlan &p, int *status) {
   Args a{};
   a.padded = p.padded;
+  a.counts = p.counts;
   a.tile_expert = p.tile_expert;
   a.pair_start = p.pair_start;
   a.pair_expert = p.pair_expert;

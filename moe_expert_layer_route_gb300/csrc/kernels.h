@@ -59,6 +59,7 @@ cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *
 //                                                        B = Y [R x N] MN-major
 struct GemmPlan {
   const int32_t *padded;       // [E+1] padded segment starts
+  const int32_t *counts;       // [E] rows per expert
   const int32_t *tile_expert;  // [R/128] expert of each 128-row tile
   const int32_t *pair_start;   // [E+1] first 256-row pair-tile of each expert
   const int32_t *pair_expert;  // [R/128] expert of each pair-tile

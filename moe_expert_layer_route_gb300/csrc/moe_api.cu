@@ -264,7 +264,7 @@ moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts
   int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
   MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
                        st));
-  const GemmPlan p{padded, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
+  const GemmPlan p{padded, counts, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, (int)s.d, (int)s.f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, (int)s.d, (int)s.f, status, st));
   return MOE_OK;
@@ -307,7 +307,7 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
                        st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
                           (int)padded_rows(s), st));
-  const GemmPlan p{padded, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
+  const GemmPlan p{padded, counts, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));
   MOE_CUDA(launch_combine(o, w, row_of, y, T, d, k, st));
@@ -339,7 +339,7 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   const int32_t *ids = at<int32_t>(fws, L.ids);
   int *status = at<int>(scratch, B.status);
   void *g = at<void>(scratch, B.g), *dgu = at<void>(scratch, B.dgu), *dxp = at<void>(scratch, B.dxp);
-  const GemmPlan p{padded, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
+  const GemmPlan p{padded, counts, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, o, ids,
                                 s.T > 0 ? dlogits : nullptr, st));
@@ -367,7 +367,7 @@ moe_status moe_debug_gate_up_withheld(moe_shape s, const moe_bf16 *xp, const int
   int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
   MOE_CUDA(launch_plan(counts, (int)s.E, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
                        st));
-  GemmPlan p{padded, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
+  GemmPlan p{padded, counts, tiles, pstart, pexp, (int)s.E, padded_rows(s), s.T * s.k / s.E};
   p.wait_ns = 1000ull * (unsigned long long)wait_limit_us;
   p.withhold_kblock = 0;
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, nullptr, (int)s.d, (int)s.f, status, st));
