@@ -48,14 +48,19 @@ def _sigmoid(z: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- route
-def route(logits: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
+def route(logits: np.ndarray, k: int, bias: np.ndarray | None = None
+          ) -> tuple[np.ndarray, np.ndarray]:
     """Per-token top-k over the router logits, then softmax over the k chosen.
 
     Follows Figure 3 ("per-token top-k router") and the fp32 router of "Where the
     gap actually is" in "Halo's 2.8x over TRL is not a kernel". Experts are ordered
-    by (logit descending, expert index ascending); the first k are the token's
-    slots. The selection compares the fp32 logits themselves, so it is exact.
-    w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen logits.
+    by (score descending, expert index ascending); the first k are the token's
+    slots. The score is the fp32 logit, or, with a selection bias (the
+    "bias_update" balancing of the LFM2 recipe in the same article: balancing
+    "through the expert-selection bias"), the fp32 sum logit + bias[e]. The
+    selection compares fp32 values, so it is exact. The weights use the unbiased
+    logits of the chosen experts: w[t, j] = exp(l_j - m) / sum_i exp(l_i - m),
+    m the largest chosen logit.
 
     Returns ids [T, k] int32 and w [T, k] float64.
     """
@@ -65,13 +70,48 @@ def route(logits: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
         raise ValueError("need 1 <= k <= E")
     if not np.all(np.isfinite(logits)):
         raise ValueError("router logits must be finite")
-    # a stable sort on the negated logits keeps equal logits in index order
-    order = np.argsort(-logits, axis=1, kind="stable")
+    score = logits
+    if bias is not None:
+        bias = np.asarray(bias, dtype=np.float32)
+        if bias.shape != (E,) or not np.all(np.isfinite(bias)):
+            raise ValueError("selection bias must be E finite values")
+        score = logits + bias[None, :]          # fp32 addition, as the score is defined
+    # a stable sort on the negated scores keeps equal scores in index order
+    order = np.argsort(-score, axis=1, kind="stable")
     ids = order[:, :k].astype(np.int32)
     chosen = np.take_along_axis(logits, ids, axis=1).astype(F64)
-    z = np.exp(chosen - chosen[:, :1])
+    z = np.exp(chosen - chosen.max(axis=1, keepdims=True))
     w = z / z.sum(axis=1, keepdims=True)
     return ids, w
+
+
+def aux_stats(logits: np.ndarray, counts: np.ndarray, k: int) -> dict:
+    """Load-balancing statistics of one routing.
+
+    The TorchTurbo adapter (its "Adapter" section) has routers apply an auxiliary
+    loss (moe.aux_loss_coeff) and report aux_loss. Reading: the usual balancing loss
+    aux = E * sum_e f_e * P_e with f_e = counts_e / (T k), the fraction of the
+    assignments that went to expert e, and P_e the mean over tokens of the softmax
+    over all E unbiased logits.
+    """
+    logits = np.asarray(logits, dtype=F64)
+    T, E = logits.shape
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    f = np.asarray(counts, dtype=F64) / (T * k)
+    P = p.mean(axis=0)
+    return {"f": f, "P": P, "aux": float(E * (f * P).sum())}
+
+
+def aux_loss_grad(logits: np.ndarray, counts: np.ndarray, k: int) -> np.ndarray:
+    """d aux / d logits with f held constant (it counts discrete choices):
+    d aux / d l[t, e] = (E / T) * p[t, e] * (f_e - sum_e' f_e' p[t, e'])."""
+    logits = np.asarray(logits, dtype=F64)
+    T, E = logits.shape
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    f = np.asarray(counts, dtype=F64) / (T * k)
+    return (E / T) * p * (f[None, :] - (p * f[None, :]).sum(axis=1, keepdims=True))
 
 
 # -------------------------------------------------------------------------- dispatch
@@ -174,11 +214,11 @@ def combine(o: np.ndarray, w: np.ndarray, row_of: np.ndarray) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------- forward
-def forward(x, logits, w_gu, w_down, k: int) -> dict:
+def forward(x, logits, w_gu, w_down, k: int, bias=None) -> dict:
     """The whole block: route, dispatch, experts, combine. Returns every stage."""
     x = np.asarray(x, dtype=F64)
     E = np.asarray(w_gu).shape[0]
-    ids, w = route(logits, k)
+    ids, w = route(logits, k, bias)
     disp = dispatch(ids, E)
     xp = permute_rows(x, disp["tok_of"])
     ffn = expert_ffn(xp, disp["offsets"], w_gu, w_down)

@@ -23,8 +23,11 @@ import workloads
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "route_dispatch_worked.json")
 
 
-def _closed_form(expr: str) -> float:
-    return float(eval(expr, {"__builtins__": {}}, {"exp": math.exp}))
+def _closed_form(expr) -> float:
+    if isinstance(expr, (int, float)):
+        return float(expr)
+    return float(eval(expr.replace("ln3", "log(3)"), {"__builtins__": {}},
+                      {"exp": math.exp, "log": math.log}))
 
 
 def _tiny(T=24, d=16, E=6, k=3, f=8, seed=11, logit_scale=1.0):
@@ -41,6 +44,68 @@ def test_route_golden_worked_examples():
         assert ids[0].tolist() == case["ids"], case["why"]
         want = np.array([_closed_form(s) for s in case["w"]])
         np.testing.assert_allclose(w[0], want, rtol=1e-14, atol=0, err_msg=case["why"])
+
+
+def test_route_bias_golden_worked_examples():
+    g = json.load(open(GOLDEN))
+    for case in g["route_bias"]:
+        ids, w = oracle.route(np.array([case["logits"]], dtype=np.float32), case["k"],
+                              np.array(case["bias"], dtype=np.float32))
+        assert ids[0].tolist() == case["ids"], case["why"]
+        want = np.array([_closed_form(x) for x in case["w"]])
+        np.testing.assert_allclose(w[0], want, rtol=1e-14, atol=0, err_msg=case["why"])
+
+
+def test_route_bias_zero_and_dominance():
+    rng = np.random.default_rng(31)
+    logits = rng.standard_normal((200, 16)).astype(np.float32)
+    for k in (1, 4):
+        a = oracle.route(logits, k)
+        b = oracle.route(logits, k, np.zeros(16, dtype=np.float32))
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    bias = (rng.integers(-4, 5, size=16) * 0.5).astype(np.float32)
+    ids, w = oracle.route(logits, 4, bias)
+    score = logits + bias
+    for t in range(200):
+        chosen = set(ids[t].tolist())
+        for i in chosen:
+            for j in set(range(16)) - chosen:
+                assert score[t, i] > score[t, j] or (score[t, i] == score[t, j] and i < j)
+        lc = logits[t, ids[t]].astype(np.float64)       # weights ignore the bias
+        np.testing.assert_allclose(w[t], scipy.special.softmax(lc), rtol=1e-13)
+
+
+def test_aux_stats_golden_worked_examples():
+    g = json.load(open(GOLDEN))
+    for case in g["aux"]:
+        logits = np.array([[_closed_form(v) for v in row] for row in case["logits"]],
+                          dtype=np.float64)
+        st = oracle.aux_stats(logits, np.array(case["counts"]), case["k"])
+        np.testing.assert_allclose(st["f"], [_closed_form(v) for v in case["f"]], atol=1e-15)
+        np.testing.assert_allclose(st["P"], [_closed_form(v) for v in case["P"]], rtol=1e-14)
+        assert abs(st["aux"] - _closed_form(case["aux"])) < 1e-14, case["why"]
+    # the counts of the golden examples are what the router chooses on those logits
+    for case in g["aux"]:
+        logits = np.array([[_closed_form(v) for v in row] for row in case["logits"]],
+                          dtype=np.float32)
+        ids, _ = oracle.route(logits, case["k"])
+        assert np.bincount(ids.ravel(), minlength=len(case["counts"])).tolist() == case["counts"]
+
+
+def test_aux_loss_grad_matches_finite_differences():
+    rng = np.random.default_rng(32)
+    logits = rng.standard_normal((7, 5))
+    counts = np.array([3, 0, 5, 4, 2])
+    g = oracle.aux_loss_grad(logits, counts, 2)
+    h = 1e-6
+    for t in range(7):
+        for e in range(5):
+            lp, lm = logits.copy(), logits.copy()
+            lp[t, e] += h
+            lm[t, e] -= h
+            fd = (oracle.aux_stats(lp, counts, 2)["aux"] - oracle.aux_stats(lm, counts, 2)["aux"]) / (2 * h)
+            assert abs(fd - g[t, e]) <= 1e-8, (t, e, fd, g[t, e])
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
 
 
 def test_route_selection_property():
