@@ -121,6 +121,7 @@ def kernel_work(wl: workloads.Workload) -> dict:
         "combine": ("byte", A * d * 2 + A * 8 + T * d * 2),
         "g_scatter": ("byte", T * d * 2 + A * d * 2 + A * 8),
         "g_scatter_router_grad": ("byte", T * d * 2 + 2 * A * d * 2 + A * 12 + T * E * 4),
+        "aux_grad": ("byte", 2 * T * E * 4 + T * E * 4),
         "dx_gather": ("byte", A * d * 2 + A * 4 + T * d * 2),
     }
 
@@ -259,13 +260,22 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     scratch = moe.new_scratch(s, dev)
     y = torch.empty_like(x)
     grads = (torch.empty_like(x), torch.empty_like(w_gu), torch.empty_like(w_down))
-    dlogits = torch.empty_like(logits) if args.router_grad else None
+    router_grad = args.router_grad or args.aux_loss
+    dlogits = torch.empty_like(logits) if router_grad else None
+    sel_bias = torch.from_numpy(workloads.zipf_bias(wl.E)).to(dev) if args.selection_bias else None
+    aux = torch.empty(2 * wl.E + 1, dtype=torch.float32, device=dev) if args.aux_loss else None
+    views = None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y)
+        moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y,
+                    bias=sel_bias, aux_stats=aux)
         if wl.backward:
             moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads, dlogits=dlogits)
+            if aux is not None:
+                moe.aux_loss_backward(s, logits, views["counts"], 0.01, dlogits)
+
+    views = moe.workspace_views(s, wl.backward, ws)
 
     for _ in range(args.warmup):
         step()
@@ -395,7 +405,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                    "f": wl.f, "seed": wl.seed,
                    "passes": ("forward+backward" if wl.backward else "forward")
-                   + (" + router-logit gradient" if args.router_grad and wl.backward else ""),
+                   + (" + router-logit gradient" if router_grad and wl.backward else "")
+                   + (" + selection bias (Zipf)" if args.selection_bias else "")
+                   + (" + load-balancing statistics and gradient" if args.aux_loss else ""),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed (256 MB write) before each timed step, outside its events; "
                          f"weights alone are {6 * wl.E * wl.d * wl.f / 1e9:.2f} GB"},
@@ -463,6 +475,11 @@ def main(argv=None) -> int:
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--router-grad", action="store_true",
                     help="also compute the router-logit gradient in the backward")
+    ap.add_argument("--selection-bias", action="store_true",
+                    help="route on logits + a per-expert selection bias (Zipf ranks)")
+    ap.add_argument("--aux-loss", action="store_true",
+                    help="load-balancing statistics in the forward, their gradient in the "
+                         "backward (implies --router-grad)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (profiling a smaller case; not a headline line)")
     ap.add_argument("--experts", type=int, default=None,

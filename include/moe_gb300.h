@@ -110,15 +110,35 @@ typedef struct {
 moe_status moe_workspace_views(moe_shape s, int training, void *ws, size_t ws_bytes,
                                moe_forward_views *out);
 
+/* Options of the routing step; a NULL options pointer or NULL fields give the plain
+ * top-k.
+ *   selection_bias [E] fp32 in: the experts are chosen by the fp32 score
+ *     logit + selection_bias[e] (descending, ties to the lower index) while the
+ *     weights stay the softmax over the chosen experts' unbiased logits; the
+ *     "bias_update" balancing of the LFM2 recipe in "Halo's 2.8x over TRL is not a
+ *     kernel" ("The small-hardware end": LFM2 balances "through the expert-selection
+ *     bias").
+ *   aux_stats [2E + 1] fp32 out (moe_forward only): load-balancing statistics for the
+ *     TorchTurbo adapter's auxiliary loss ("Adapter": aux_loss_coeff, aux_loss):
+ *     aux_stats[e] = f_e = counts_e / (T k), aux_stats[E + e] = P_e = the mean over
+ *     tokens of the softmax over all E logits, aux_stats[2E] = E * sum_e f_e P_e.
+ *     Reduced in a fixed order (deterministic). */
+typedef struct {
+  const float *selection_bias;
+  float *aux_stats;
+} moe_route_options;
+
 /* Route. "Halo's 2.8x over TRL is not a kernel", Figure 3 and "Where the gap
  * actually is": per-token top-k router on fp32 logits, outputs weighted by the
  * top-k probabilities.
- *   logits [T x E] fp32 in; ids [T x k] int32 out; w [T x k] fp32 out.
- * ids[t][0..k-1] are the k experts with the largest logits, ordered by descending
- * logit, equal logits by ascending expert index (the lower index wins a tie).
- * w[t][j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen logits.
- * One warp per token. No workspace. */
-moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w, moe_stream stream);
+ *   logits [T x E] fp32 in; ids [T x k] int32 out; w [T x k] fp32 out;
+ *   opts: see moe_route_options (aux_stats is ignored here) or NULL.
+ * ids[t][0..k-1] are the k experts with the largest scores (the logits, or
+ * logits + selection bias), ordered by descending score, equal scores by ascending
+ * expert index (the lower index wins a tie). w[t][j] = exp(l_j - m) / sum_i exp(l_i - m)
+ * over the k chosen unbiased logits, m their largest. One warp per token. */
+moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w,
+                     const moe_route_options *opts, moe_stream stream);
 
 /* Dispatch. Figure 3 of "Halo's 2.8x over TRL is not a kernel": tokens sorted by
  * expert for a grouped matmul. A stable counting sort of the assignments
@@ -165,10 +185,22 @@ moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int
  * (see moe_workspace_views). training != 0 also keeps GU for moe_backward; ws must
  * then hold moe_workspace_size(s, 1) bytes and outlive the matching moe_backward.
  *   x [T x d] bf16; logits [T x E] fp32; w_gu [E x d x 2f] bf16; w_down [E x f x d] bf16;
- *   y [T x d] bf16 out. */
+ *   y [T x d] bf16 out; opts: see moe_route_options, or NULL. */
 moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
-                       const moe_bf16 *w_down, moe_bf16 *y, int training, void *ws,
-                       size_t ws_bytes, moe_stream stream);
+                       const moe_bf16 *w_down, moe_bf16 *y, int training,
+                       const moe_route_options *opts, void *ws, size_t ws_bytes,
+                       moe_stream stream);
+
+/* Gradient of the load-balancing loss coeff * aux (see moe_route_options) with respect
+ * to the router logits, ADDED into dlogits, with the assignment fractions f held
+ * fixed (they count discrete choices):
+ *   dlogits[t][e] += coeff * (E / T) * p[t][e] * (f_e - sum_e' f_e' p[t][e'])
+ * where p[t] is the softmax over all E logits of token t and f_e = counts[e] / (T k).
+ * One warp per token; every element read and written by one thread.
+ *   logits [T x E] fp32 in; counts [E] int32 in (from the forward); dlogits [T x E]
+ *   fp32 in/out. */
+moe_status moe_aux_loss_backward(moe_shape s, const float *logits, const int32_t *counts,
+                                 float coeff, float *dlogits, moe_stream stream);
 
 /* Backward of the block for dY ("Halo: Frontier-Lab Training for Everyone", "The hard
  * problems along the way": an atomic-free routing backward). With

@@ -33,6 +33,10 @@ class _Views(ctypes.Structure):
                                      "tok_of", "xp", "gu", "h", "o")]
 
 
+class _RouteOptions(ctypes.Structure):
+    _fields_ = [("selection_bias", _c_vp), ("aux_stats", _c_vp)]
+
+
 class _LaunchTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("ms", ctypes.c_float)]
 
@@ -49,7 +53,8 @@ _SIG = {
     "moe_backward_scratch_size": (ctypes.c_size_t, [MoEShape]),
     "moe_workspace_views": (ctypes.c_int, [MoEShape, ctypes.c_int, _c_vp, ctypes.c_size_t,
                                            ctypes.POINTER(_Views)]),
-    "moe_route": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "moe_route": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, ctypes.POINTER(_RouteOptions),
+                                 _c_vp]),
     "moe_dispatch": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                     _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_expert_ffn": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -58,7 +63,8 @@ _SIG = {
     "moe_dispatch_noalloc": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                             _c_vp, _c_vp, _c_vp]),
     "moe_forward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_int,
-                                   _c_vp, ctypes.c_size_t, _c_vp]),
+                                   ctypes.POINTER(_RouteOptions), _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_aux_loss_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "moe_check_device_status": (ctypes.c_int, [_c_vp, _c_vp]),
@@ -194,14 +200,26 @@ def workspace_views(s: MoEShape, training: bool, ws: torch.Tensor) -> dict:
 
 
 # ------------------------------------------------------------------------- the stages
-def route(logits: torch.Tensor, k: int) -> tuple[torch.Tensor, torch.Tensor]:
-    """moe_route: ids [T,k] int32, w [T,k] fp32."""
+def _options(bias: torch.Tensor | None, aux: torch.Tensor | None):
+    if bias is None and aux is None:
+        return None
+    if bias is not None:
+        _want(bias, torch.float32, "selection bias")
+    if aux is not None:
+        _want(aux, torch.float32, "aux_stats")
+    return ctypes.byref(_RouteOptions(_p(bias), _p(aux)))
+
+
+def route(logits: torch.Tensor, k: int, bias: torch.Tensor | None = None
+          ) -> tuple[torch.Tensor, torch.Tensor]:
+    """moe_route: ids [T,k] int32, w [T,k] fp32 (bias: optional [E] selection bias)."""
     _want(logits, torch.float32, "logits")
     T, E = logits.shape
     ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
     s = shape(T, 8, E, k, 8)
-    _check(lib().moe_route(s, _p(logits), _p(ids), _p(w), _stream()), "moe_route")
+    _check(lib().moe_route(s, _p(logits), _p(ids), _p(w), _options(bias, None), _stream()),
+           "moe_route")
     return ids, w
 
 
@@ -275,8 +293,10 @@ def combine(s: MoEShape, o: torch.Tensor, w: torch.Tensor, row_of: torch.Tensor)
 
 def forward(x: torch.Tensor, logits: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Tensor,
             k: int, training: bool = False, ws: torch.Tensor | None = None,
-            y: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor, MoEShape]:
-    """moe_forward: returns (y, workspace, shape); the workspace feeds backward()."""
+            y: torch.Tensor | None = None, bias: torch.Tensor | None = None,
+            aux_stats: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor, MoEShape]:
+    """moe_forward: returns (y, workspace, shape); the workspace feeds backward().
+    bias: optional [E] selection bias; aux_stats: optional [2E+1] fp32 output."""
     _want(x, torch.bfloat16, "x")
     _want(logits, torch.float32, "logits")
     T, d = x.shape
@@ -287,8 +307,20 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w_gu: torch.Tensor, w_down: t
     if y is None:
         y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     _check(lib().moe_forward(s, _p(x), _p(logits), _p(w_gu), _p(w_down), _p(y), int(bool(training)),
-                             _p(ws), ws.numel(), _stream()), "moe_forward")
+                             _options(bias, aux_stats), _p(ws), ws.numel(), _stream()),
+           "moe_forward")
     return y, ws, s
+
+
+def aux_loss_backward(s: MoEShape, logits: torch.Tensor, counts: torch.Tensor, coeff: float,
+                      dlogits: torch.Tensor) -> torch.Tensor:
+    """moe_aux_loss_backward: adds coeff * d aux / d logits into dlogits (in place)."""
+    _want(logits, torch.float32, "logits")
+    _want(counts, torch.int32, "counts")
+    _want(dlogits, torch.float32, "dlogits")
+    _check(lib().moe_aux_loss_backward(s, _p(logits), _p(counts), float(coeff), _p(dlogits),
+                                       _stream()), "moe_aux_loss_backward")
+    return dlogits
 
 
 def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Tensor,
@@ -352,5 +384,5 @@ def launch_count() -> int:
 
 __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
-           "dispatch", "dispatch_noalloc", "expert_ffn", "combine", "forward", "backward", "check_device_status", "debug_gate_up_withheld",
+           "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward", "combine", "forward", "backward", "check_device_status", "debug_gate_up_withheld",
            "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

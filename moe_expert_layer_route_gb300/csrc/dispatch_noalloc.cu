@@ -91,8 +91,8 @@ extern "C" moe_status moe_dispatch_noalloc(moe_shape s, const moe_bf16 *x, const
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d;
   if (moe::launch_count(ids, rank, hist, T, E, k, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_scan(hist, T, E, counts, offsets, padded_offsets, tiles, nullptr, nullptr, st) !=
-      cudaSuccess)
+  if (moe::launch_scan(hist, T, E, k, counts, offsets, padded_offsets, tiles, nullptr, nullptr,
+                       nullptr, nullptr, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_scatter(x, ids, rank, hist, padded_offsets, counts, row_of, tok_of, xp, T, d, E,
                           k, (int)R, st) != cudaSuccess)

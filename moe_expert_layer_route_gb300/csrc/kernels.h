@@ -18,14 +18,21 @@ void launch_begin(cudaStream_t st);
 cudaError_t note_launch(const char *name, cudaStream_t st);
 
 // route_dispatch.cu
-cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *rank,
-                         int32_t *hist, int T, int E, int k, bool with_count, cudaStream_t st);
+// bias [E] (selection bias) and prob_part [E x ceil(T/32)] (per-chunk softmax sums for
+// the load-balancing statistics) may be null
+cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, float *w,
+                         int32_t *rank, int32_t *hist, float *prob_part, int T, int E, int k,
+                         bool with_count, cudaStream_t st);
+cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,
+                            float *dlogits, int T, int E, int k, cudaStream_t st);
 cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,
                          cudaStream_t st);
-// pair_start / pair_expert may be null (then only the 128-row tile table is written)
-cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
+// pair_start / pair_expert may be null (then only the 128-row tile table is written);
+// with prob_part also aux = [f_e (E), P_e (E), E * sum f_e P_e]
+cudaError_t launch_scan(int32_t *hist, int T, int E, int k, int32_t *counts, int32_t *offsets,
                         int32_t *padded, int32_t *tile_expert, int32_t *pair_start,
-                        int32_t *pair_expert, cudaStream_t st);
+                        int32_t *pair_expert, const float *prob_part, float *aux,
+                        cudaStream_t st);
 cudaError_t launch_plan(const int32_t *counts, int E, int32_t *offsets, int32_t *padded,
                         int32_t *tile_expert, int32_t *pair_start, int32_t *pair_expert,
                         cudaStream_t st);

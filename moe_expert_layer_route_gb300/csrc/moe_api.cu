@@ -16,8 +16,8 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct FwdLayout {
-  size_t status, ids, w, rank, hist, counts, offsets, padded, tile_expert, pair_start, pair_expert,
-      row_of, tok_of, xp, gu, h, o, total;
+  size_t status, ids, w, rank, hist, prob_part, counts, offsets, padded, tile_expert, pair_start,
+      pair_expert, row_of, tok_of, xp, gu, h, o, total;
 };
 
 struct BwdLayout {
@@ -44,6 +44,7 @@ FwdLayout fwd_layout(const moe_shape &s, int training) {
   L.w = take(A * 4);
   L.rank = take(A * 4);
   L.hist = take((size_t)s.E * C * 4);
+  L.prob_part = take((size_t)s.E * C * 4);
   L.counts = take(s.E * 4);
   L.offsets = take((s.E + 1) * 4);
   L.padded = take((s.E + 1) * 4);
@@ -215,14 +216,17 @@ moe_status moe_workspace_views(moe_shape s, int training, void *ws, size_t ws_by
   return MOE_OK;
 }
 
-moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w, moe_stream stream) {
+moe_status moe_route(moe_shape s, const float *logits, int32_t *ids, float *w,
+                     const moe_route_options *opts, moe_stream stream) {
   MOE_TRY(check_shape(s));
+  const float *bias = opts ? opts->selection_bias : nullptr;
+  if (bias && !aligned16(bias)) return MOE_ERR_ALIGNMENT;
   if (s.T == 0) return MOE_OK;
   MOE_TRY(check_ptrs(logits, ids, w));
   MOE_TRY(check_device());
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_route(logits, ids, w, nullptr, nullptr, (int)s.T, (int)s.E, (int)s.k, false,
-                        st));
+  MOE_CUDA(launch_route(logits, bias, ids, w, nullptr, nullptr, nullptr, (int)s.T, (int)s.E,
+                        (int)s.k, false, st));
   return MOE_OK;
 }
 
@@ -240,8 +244,8 @@ moe_status moe_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_
   const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d;
   int32_t *rank = at<int32_t>(ws, L.rank), *hist = at<int32_t>(ws, L.hist);
   MOE_CUDA(launch_count(ids, rank, hist, T, E, k, st));
-  MOE_CUDA(launch_scan(hist, T, E, counts, offsets, padded_offsets, at<int32_t>(ws, L.tile_expert),
-                       nullptr, nullptr, st));
+  MOE_CUDA(launch_scan(hist, T, E, k, counts, offsets, padded_offsets,
+                       at<int32_t>(ws, L.tile_expert), nullptr, nullptr, nullptr, nullptr, st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded_offsets, counts, row_of, tok_of, xp, T, d, E,
                           k, (int)padded_rows(s), st));
   return MOE_OK;
@@ -282,10 +286,14 @@ moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int
 }
 
 moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
-                       const moe_bf16 *w_down, moe_bf16 *y, int training, void *ws,
-                       size_t ws_bytes, moe_stream stream) {
+                       const moe_bf16 *w_down, moe_bf16 *y, int training,
+                       const moe_route_options *opts, void *ws, size_t ws_bytes,
+                       moe_stream stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(check_ptrs(w_gu, w_down, ws));
+  const float *bias = opts ? opts->selection_bias : nullptr;
+  float *aux = opts ? opts->aux_stats : nullptr;
+  if ((bias && !aligned16(bias)) || (aux && !aligned16(aux))) return MOE_ERR_ALIGNMENT;
   if (s.T > 0) MOE_TRY(check_ptrs(x, logits, y));
   const FwdLayout L = fwd_layout(s, training);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -301,10 +309,12 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   void *xp = at<void>(ws, L.xp), *h = at<void>(ws, L.h), *o = at<void>(ws, L.o);
   void *gu = training ? at<void>(ws, L.gu) : nullptr;
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
-  MOE_CUDA(launch_route(logits, ids, w, rank, hist, T, E, k, true, st));
+  float *prob_part = aux ? at<float>(ws, L.prob_part) : nullptr;
+  MOE_CUDA(launch_route(logits, bias, ids, w, rank, hist, prob_part, T, E, k, true, st));
   int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
-  MOE_CUDA(launch_scan(hist, T, E, counts, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp,
-                       st));
+  MOE_CUDA(launch_scan(hist, T, E, k, counts, at<int32_t>(ws, L.offsets), padded, tiles, pstart,
+                       pexp, prob_part, aux, st));
+  if (aux && T == 0) MOE_CUDA(cudaMemsetAsync(aux, 0, (2 * E + 1) * sizeof(float), st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
                           (int)padded_rows(s), st));
   const GemmPlan p{padded, counts, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
@@ -348,6 +358,17 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   MOE_CUDA(gemm_dgrad_x(p, dgu, w_gu, dxp, d, f, status, st));
   MOE_CUDA(gemm_wgrad(p, xp, dgu, dw_gu, d, 2 * f, status, "gemm_wgrad_gu", st));
   MOE_CUDA(launch_gather_sum(dxp, row_of, dx, T, d, k, st));
+  return MOE_OK;
+}
+
+moe_status moe_aux_loss_backward(moe_shape s, const float *logits, const int32_t *counts,
+                                 float coeff, float *dlogits, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(logits, counts, dlogits));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_aux_grad(logits, counts, coeff, dlogits, (int)s.T, (int)s.E, (int)s.k,
+                           static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

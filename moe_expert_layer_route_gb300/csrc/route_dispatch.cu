@@ -19,19 +19,26 @@ constexpr int kVec = 4;           // 16-byte vectors each lane keeps in flight i
 
 // ---------------------------------------------------------------------------- route
 // One warp per token. Lane l holds logits l, l+32, ... (E <= 256, so <= 8 each).
-// k rounds of a warp arg-max under the order (logit descending, index ascending);
-// lane j keeps slot j. Weights: softmax over the k chosen logits in fp32.
-__device__ __forceinline__ void route_one_token(const float *__restrict__ row, int E, int k,
-                                                int lane, int &slot_id, float &slot_w) {
-  float v[8];
+// k rounds of a warp arg-max of the score under the order (score descending, index
+// ascending); lane j keeps slot j. The score is the logit, or logit + bias[e] in fp32
+// with a selection bias. Weights: softmax over the k chosen unbiased logits in fp32.
+// With prob (aux statistics) the lane also returns the full softmax over all E
+// unbiased logits for its experts.
+__device__ __forceinline__ void route_one_token(const float *__restrict__ row,
+                                                const float *__restrict__ bias, int E, int k,
+                                                int lane, int &slot_id, float &slot_w,
+                                                float (*prob)[8]) {
+  float v[8], sc[8];
   uint32_t taken = 0;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int e = lane + 32 * q;
     v[q] = (e < E) ? __ldg(row + e) : 0.f;
+    sc[q] = (e < E && bias) ? v[q] + __ldg(bias + e) : v[q];
     if (e >= E) taken |= 1u << q;
   }
-  float my_v = 0.f;
+  const uint32_t valid = ~taken & 0xffu;
+  float my_l = 0.f;
   int my_i = -1;
   for (int j = 0; j < k; ++j) {
     float bv = 0.f;
@@ -40,8 +47,8 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ row, i
     for (int q = 0; q < 8; ++q) {
       if (!((taken >> q) & 1u)) {
         // candidates in ascending index: strict '>' keeps the lower index on ties
-        if (bi == 0x7fffffff || v[q] > bv) {
-          bv = v[q];
+        if (bi == 0x7fffffff || sc[q] > bv) {
+          bv = sc[q];
           bi = lane + 32 * q;
         }
       }
@@ -57,19 +64,45 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ row, i
         bi = oi;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const bool mine = (bi & 31) == lane;
+    float lv = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (mine && (bi >> 5) == q) lv = v[q];
+    lv = __shfl_sync(0xffffffffu, lv, bi & 31);  // the chosen expert's unbiased logit
+    if (mine) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      my_v = bv;
+      my_l = lv;
       my_i = bi;
     }
   }
-  const float m = __shfl_sync(0xffffffffu, my_v, 0);
-  const float z = (lane < k) ? expf(my_v - m) : 0.f;
+  float m = (lane < k) ? my_l : -INFINITY;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float z = (lane < k) ? expf(my_l - m) : 0.f;
   float s = z;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   slot_id = my_i;
   slot_w = z / s;
+  if (prob) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if ((valid >> q) & 1u) mx = fmaxf(mx, v[q]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float ex[8], sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      ex[q] = ((valid >> q) & 1u) ? expf(v[q] - mx) : 0.f;
+      sum += ex[q];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) (*prob)[q] = ex[q] / sum;
+  }
 }
 
 // Ballot count of one chunk of 32 tokens: for each expert, the number of tokens of
@@ -94,33 +127,52 @@ __device__ __forceinline__ void count_chunk(const int32_t (*s_ids)[kMaxK], int c
 }
 
 // Block c routes tokens [32c, 32c+32), one warp per token, and, when COUNT, also
-// writes the chunk histogram and local ranks for the dispatch.
+// writes the chunk histogram and local ranks for the dispatch. With prob_part it also
+// writes prob_part[e][c], the sum over the chunk's tokens (in token order) of the
+// softmax of all E logits, for the load-balancing statistics.
 template <bool COUNT>
 __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ logits,
-                                                    int32_t *__restrict__ ids,
-                                                    float *__restrict__ w,
-                                                    int32_t *__restrict__ rank,
-                                                    int32_t *__restrict__ hist, int T, int E,
-                                                    int k, int C) {
+                                                     const float *__restrict__ bias,
+                                                     int32_t *__restrict__ ids,
+                                                     float *__restrict__ w,
+                                                     int32_t *__restrict__ rank,
+                                                     int32_t *__restrict__ hist,
+                                                     float *__restrict__ prob_part, int T, int E,
+                                                     int k, int C) {
   __shared__ int32_t s_ids[kChunk][kMaxK];
+  __shared__ float s_prob[kChunk][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   for (int i = warp; i < kChunk; i += 32) {
     const int t = c * kChunk + i;
-    if (t >= T) break;
+    if (t >= T) {
+      if (prob_part)
+        for (int e = lane; e < E; e += 32) s_prob[i][e] = 0.f;
+      break;
+    }
     int sid;
-    float sw;
-    route_one_token(logits + (int64_t)t * E, E, k, lane, sid, sw);
+    float sw, pr[8];
+    route_one_token(logits + (int64_t)t * E, bias, E, k, lane, sid, sw, prob_part ? &pr : nullptr);
     if (lane < k) {
       ids[(int64_t)t * k + lane] = sid;
       w[(int64_t)t * k + lane] = sw;
       s_ids[i][lane] = sid;
     }
+    if (prob_part) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (lane + 32 * q < E) s_prob[i][lane + 32 * q] = pr[q];
+    }
   }
-  if constexpr (COUNT) {
-    __syncthreads();
-    count_chunk(s_ids, c, T, E, k, C, warp, 32, lane, rank, hist);
+  if (COUNT || prob_part) __syncthreads();
+  if (prob_part) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float acc = 0.f;
+      for (int i = 0; i < kChunk; ++i) acc += s_prob[i][e];
+      prob_part[(int64_t)e * C + c] = acc;
+    }
   }
+  if constexpr (COUNT) count_chunk(s_ids, c, T, E, k, C, warp, 32, lane, rank, hist);
 }
 
 // Histogram and local ranks from ids already in memory (standalone dispatch).
@@ -189,14 +241,20 @@ __device__ void plan_from_counts(const int32_t *s_cnt, int E, int32_t *__restric
   }
 }
 
+// With prob_part, also the load-balancing statistics: aux[e] = f_e = counts_e / (T k),
+// aux[E + e] = P_e = (sum over chunks, in chunk order, of prob_part[e][c]) / T and
+// aux[2E] = E * sum_e f_e P_e (summed in expert order).
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, int C, int E,
                                                     int32_t *__restrict__ counts,
                                                     int32_t *__restrict__ offsets,
                                                     int32_t *__restrict__ padded,
                                                     int32_t *__restrict__ tile_expert,
                                                     int32_t *__restrict__ pair_start,
-                                                    int32_t *__restrict__ pair_expert) {
+                                                    int32_t *__restrict__ pair_expert,
+                                                    const float *__restrict__ prob_part,
+                                                    float *__restrict__ aux, int T, int k) {
   __shared__ int32_t s_cnt[kMaxE];
+  __shared__ float s_p[kMaxE];
   __shared__ int32_t s_pad[kMaxE + 1];
   __shared__ int32_t s_pair[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -219,8 +277,25 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
       s_cnt[e] = running;
       counts[e] = running;
     }
+    if (prob_part) {
+      float acc = 0.f;  // lane-strided chunks, then a fixed butterfly: a fixed order
+      for (int c = lane; c < C; c += 32) acc += prob_part[(int64_t)e * C + c];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) s_p[e] = acc / (float)T;
+    }
   }
   __syncthreads();
+  if (prob_part && threadIdx.x == 0) {
+    float l = 0.f;
+    for (int e = 0; e < E; ++e) {
+      const float f = (float)s_cnt[e] / ((float)T * (float)k);
+      aux[e] = f;
+      aux[E + e] = s_p[e];
+      l += f * s_p[e];
+    }
+    aux[2 * E] = (float)E * l;
+  }
   plan_from_counts(s_cnt, E, offsets, padded, tile_expert, pair_start, pair_expert, s_pad, s_pair);
 }
 
@@ -446,21 +521,81 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
   }
 }
 
+// ---------------------------------------------------------- load-balancing gradient
+// dlogits[t][e] += coeff * (E / T) * p[t][e] * (f_e - sum_e' f_e' p[t][e']), the
+// gradient of coeff * aux with the assignment fractions f held fixed (they count
+// discrete choices); p is the softmax over all E logits of token t. One warp per
+// token, each element read and written by one lane.
+__global__ void __launch_bounds__(256) aux_grad_kernel(const float *__restrict__ logits,
+                                                       const int32_t *__restrict__ counts,
+                                                       float coeff, float *__restrict__ dlogits,
+                                                       int T, int E, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float *row = logits + (int64_t)t * E;
+  float v[8], f[8];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    v[q] = (e < E) ? __ldg(row + e) : -INFINITY;
+    f[q] = (e < E) ? (float)__ldg(counts + e) / ((float)T * (float)k) : 0.f;
+    mx = fmaxf(mx, v[q]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    v[q] = (lane + 32 * q < E) ? expf(v[q] - mx) : 0.f;
+    sum += v[q];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  float fp = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    v[q] /= sum;
+    fp += f[q] * v[q];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, off);
+  const float scale = coeff * (float)E / (float)T;
+  float *out = dlogits + (int64_t)t * E;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) out[e] += scale * v[q] * (f[q] - fp);
+  }
+}
+
 // ------------------------------------------------------------------------ launchers
 static inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-cudaError_t launch_route(const float *logits, int32_t *ids, float *w, int32_t *rank,
-                         int32_t *hist, int T, int E, int k, bool with_count, cudaStream_t st) {
+cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, float *w,
+                         int32_t *rank, int32_t *hist, float *prob_part, int T, int E, int k,
+                         bool with_count, cudaStream_t st) {
   const int C = ceil_div(T, kChunk);
   if (C == 0) return cudaSuccess;
   if (with_count) {
     launch_begin(st);
-    route_kernel<true><<<C, 1024, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+    route_kernel<true><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist, prob_part, T, E, k,
+                                           C);
     return note_launch("route_count", st);
   }
   launch_begin(st);
-  route_kernel<false><<<C, 1024, 0, st>>>(logits, ids, w, rank, hist, T, E, k, C);
+  route_kernel<false><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist, prob_part, T, E, k,
+                                          C);
   return note_launch("route", st);
+}
+
+cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,
+                            float *dlogits, int T, int E, int k, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  launch_begin(st);
+  aux_grad_kernel<<<ceil_div(T, 8), 256, 0, st>>>(logits, counts, coeff, dlogits, T, E, k);
+  return note_launch("aux_grad", st);
 }
 
 cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,
@@ -472,13 +607,14 @@ cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T
   return note_launch("count", st);
 }
 
-cudaError_t launch_scan(int32_t *hist, int T, int E, int32_t *counts, int32_t *offsets,
+cudaError_t launch_scan(int32_t *hist, int T, int E, int k, int32_t *counts, int32_t *offsets,
                         int32_t *padded, int32_t *tile_expert, int32_t *pair_start,
-                        int32_t *pair_expert, cudaStream_t st) {
+                        int32_t *pair_expert, const float *prob_part, float *aux,
+                        cudaStream_t st) {
   const int C = ceil_div(T, kChunk);
   launch_begin(st);
   scan_kernel<<<1, 1024, 0, st>>>(hist, C, E, counts, offsets, padded, tile_expert, pair_start,
-                                  pair_expert);
+                                  pair_expert, T > 0 ? prob_part : nullptr, aux, T, k);
   return note_launch("scan", st);
 }
 

@@ -78,7 +78,7 @@ def test_shape_validation(moe, T, d, E, k, f, status):
     s = moe.shape(T, d, E, k, f)
     assert moe.lib().moe_workspace_size(s, 1) == 0
     fake = ctypes.c_void_p(0x10000)
-    rc = moe.lib().moe_forward(s, fake, fake, fake, fake, fake, 1, fake, 1 << 40, None)
+    rc = moe.lib().moe_forward(s, fake, fake, fake, fake, fake, 1, None, fake, 1 << 40, None)
     assert rc == status
 
 
@@ -89,9 +89,12 @@ def test_pointer_and_workspace_validation(moe):
     odd = ctypes.c_void_p(0x10008)
     null = ctypes.c_void_p(None)
     need = L.moe_workspace_size(s, 1)
-    assert L.moe_forward(s, null, good, good, good, good, 1, good, need, None) == -1
-    assert L.moe_forward(s, odd, good, good, good, good, 1, good, need, None) == -3
-    assert L.moe_forward(s, good, good, good, good, good, 1, good, need - 1, None) == -4
+    assert L.moe_forward(s, null, good, good, good, good, 1, None, good, need, None) == -1
+    assert L.moe_forward(s, odd, good, good, good, good, 1, None, good, need, None) == -3
+    assert L.moe_forward(s, good, good, good, good, good, 1, None, good, need - 1, None) == -4
+    bad_opts = moe._RouteOptions(odd, None)
+    assert L.moe_forward(s, good, good, good, good, good, 1, ctypes.byref(bad_opts), good, need,
+                         None) == -3
     scratch = L.moe_backward_scratch_size(s)
     assert L.moe_backward(s, good, good, good, good, need, good, good, good, null, good,
                           scratch - 1, None) == -4
@@ -100,7 +103,7 @@ def test_pointer_and_workspace_validation(moe):
     assert L.moe_backward(s, good, good, good, good, need, good, good, good, odd, good,
                           scratch, None) == -3
     assert L.moe_combine(s, good, good, good, null, None) == -1
-    assert L.moe_route(s, good, good, odd, None) == -3
+    assert L.moe_route(s, good, good, odd, None, None) == -3
 
 
 def test_views_follow_the_layout(moe):
