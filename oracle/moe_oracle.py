@@ -114,6 +114,36 @@ def aux_loss_grad(logits: np.ndarray, counts: np.ndarray, k: int) -> np.ndarray:
     return (E / T) * p * (f[None, :] - (p * f[None, :]).sum(axis=1, keepdims=True))
 
 
+def router_logits(x: np.ndarray, w_r: np.ndarray) -> np.ndarray:
+    """fp32 router logits: logits[t, e] = sum over i of x[t, i] * w_r[e, i].
+
+    "Halo's 2.8x over TRL is not a kernel, and its own benchmark proves it" computes
+    the router's logits in fp32 ("Where the gap actually is"; `fp32_router: true` in
+    the LFM2 recipe of "The small-hardware end"). Reading: x [T, d] and the router
+    weight w_r [E, d] (one row per expert) are bf16 values taken as fp32; the sum runs
+    over i = 0 .. d-1 in order, each step adding the exact product x[t, i] * w_r[e, i]
+    (exact in fp64: two 8-bit significands) to the fp32 partial sum with one rounding
+    to fp32. Returns [T, E] float32.
+    """
+    x = np.asarray(x, dtype=np.float32).astype(F64)
+    w_r = np.asarray(w_r, dtype=np.float32).astype(F64)
+    T, d = x.shape
+    acc = np.zeros((T, w_r.shape[0]), dtype=np.float32)
+    for i in range(d):
+        acc = (acc.astype(F64) + x[:, i:i + 1] * w_r[:, i][None, :]).astype(np.float32)
+    return acc
+
+
+def router_weight_backward(x: np.ndarray, w_r: np.ndarray, dlogits: np.ndarray
+                           ) -> tuple[np.ndarray, np.ndarray]:
+    """Gradients through the router GEMM logits = x w_r^T: dW_r = dlogits^T x [E, d]
+    and the contribution dlogits w_r [T, d] to dX (float64)."""
+    x = np.asarray(x, dtype=F64)
+    w_r = np.asarray(w_r, dtype=F64)
+    dl = np.asarray(dlogits, dtype=F64)
+    return dl.T @ x, dl @ w_r
+
+
 # -------------------------------------------------------------------------- dispatch
 def dispatch(ids: np.ndarray, E: int) -> dict:
     """Counting-sort dispatch of the T*k assignments into per-expert segments.

@@ -108,6 +108,63 @@ def test_aux_loss_grad_matches_finite_differences():
     np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
 
 
+def test_router_logits_sequential_fp32_definition():
+    """The fp32 sum runs in index order: 2^24 + 1 rounds back to 2^24 (ties to even),
+    so [1, 1, 1] . [2^24, 1, -2^24] is 0, not the exact 1; the reverse order gives 1."""
+    x = np.ones((1, 3), dtype=np.float32)
+    w = np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)]], dtype=np.float32)
+    assert oracle.router_logits(x, w)[0, 0] == 0.0
+    assert oracle.router_logits(x, w[:, ::-1])[0, 0] == 1.0
+
+
+def test_router_logits_addition_rounds_half_to_even():
+    """(1 + 2^-7)^2 = 1 + 2^-6 + 2^-14 (exact: two 8-bit significands); added to 2^10 the
+    2^-14 bit is half of the fp32 ulp there (2^-13), a tie that rounds to the even
+    neighbour, so the logit is 2^10 + 1 + 2^-6."""
+    v = np.float32(1 + 2.0 ** -7)
+    x = np.array([[1.0, v]], dtype=np.float32)
+    w = np.array([[2.0 ** 10, v]], dtype=np.float32)
+    assert oracle.router_logits(x, w)[0, 0] == np.float32(2.0 ** 10 + 1 + 2.0 ** -6)
+    assert oracle.router_logits(x, w * 2)[0, 0] == np.float32(2.0 ** 11 + 2 + 2.0 ** -5)
+
+
+def test_router_logits_exact_on_integers_and_close_to_fp64():
+    rng = np.random.default_rng(41)
+    x = rng.integers(-8, 9, size=(20, 64)).astype(np.float32)     # small integers: every
+    w = rng.integers(-8, 9, size=(6, 64)).astype(np.float32)      # partial sum is exact
+    assert np.array_equal(oracle.router_logits(x, w), x.astype(np.int64) @ w.astype(np.int64).T)
+    wl, inp = workloads.small_case(50, 256, 8, 2, 64, seed=42)
+    xb = inp.x.float().numpy()
+    wr = workloads.to_bf16(np.random.default_rng(43).standard_normal((8, 256)) * 0.05).float().numpy()
+    got = oracle.router_logits(xb, wr).astype(np.float64)
+    ref = xb.astype(np.float64) @ wr.astype(np.float64).T
+    bound = 256 * 2.0 ** -24 * (np.abs(xb).astype(np.float64) @ np.abs(wr).astype(np.float64).T)
+    assert (np.abs(got - ref) <= bound).all()
+    assert not np.array_equal(got, ref.astype(np.float32))   # the order does show
+
+
+def test_router_weight_backward_is_the_gemm_gradient():
+    rng = np.random.default_rng(44)
+    x, w = rng.standard_normal((9, 7)), rng.standard_normal((4, 7))
+    dl = rng.standard_normal((9, 4))
+    dw, dx = oracle.router_weight_backward(x, w, dl)
+    assert dw.shape == (4, 7) and dx.shape == (9, 7)
+    h = 1e-6
+    loss = lambda xx, ww: (xx @ ww.T * dl).sum()
+    for e in range(4):
+        for i in range(7):
+            wp, wm = w.copy(), w.copy()
+            wp[e, i] += h
+            wm[e, i] -= h
+            assert abs((loss(x, wp) - loss(x, wm)) / (2 * h) - dw[e, i]) < 1e-7
+    for t in range(9):
+        for i in range(7):
+            xp, xm = x.copy(), x.copy()
+            xp[t, i] += h
+            xm[t, i] -= h
+            assert abs((loss(xp, w) - loss(xm, w)) / (2 * h) - dx[t, i]) < 1e-7
+
+
 def test_route_selection_property():
     """Every chosen logit beats every unchosen one (ties: lower index wins)."""
     rng = np.random.default_rng(5)

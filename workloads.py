@@ -16,7 +16,10 @@ logits ~ N(0,1) [T,E] fp32; W_gu ~ N(0, 0.02^2) [E,d,2f]; W_down ~ N(0, 0.02^2)
 [E,f,d]; dY ~ N(0,1) [T,d] (backward configs only). x, W_gu, W_down and dY are
 rounded to bf16; logits stay fp32. The skewed workload adds a per-expert bias
 3*ln(p_e) to every logit row, p_e the Zipf(s=1.2) probability of rank e+1 over
-E ranks, so expert 0 is the most popular.
+E ranks, so expert 0 is the most popular. Where the router GEMM computes the
+logits from x, its weight W_r ~ N(0, 1/d) [E,d] (unit-variance logits) is rounded
+to bf16 and drawn from a stream of its own (seed sequence [seed, 7]), so adding it
+changes none of the draws above.
 """
 from __future__ import annotations
 
@@ -130,6 +133,12 @@ def make_inputs(wl: Workload, with_dy: bool | None = None) -> Inputs:
                   w_gu=w_gu, w_down=w_down, dy=dy)
 
 
+def make_router_weight(wl: Workload) -> torch.Tensor:
+    """Router weight [E, d] bf16, one row per expert, N(0, 1/d)."""
+    rng = np.random.default_rng([wl.seed, 7])
+    return _normal_bf16(rng, (wl.E, wl.d), 1.0 / np.sqrt(wl.d))
+
+
 def small_case(T: int, d: int, E: int, k: int, f: int, seed: int, backward: bool = True,
                logit_scale: float = 1.0) -> tuple[Workload, Inputs]:
     """An ad-hoc shape drawn with the same recipe (for parity and edge-case tests)."""
@@ -142,4 +151,4 @@ def small_case(T: int, d: int, E: int, k: int, f: int, seed: int, backward: bool
 
 
 __all__ = ["Workload", "WORKLOADS", "Inputs", "make_inputs", "small_case", "to_bf16",
-           "zipf_bias"]
+           "zipf_bias", "make_router_weight"]
