@@ -191,6 +191,32 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
                        const moe_route_options *opts, void *ws, size_t ws_bytes,
                        moe_stream stream);
 
+/* Router GEMM with the route in its epilogue. "Halo's 2.8x over TRL is not a kernel":
+ * the router logits are computed in fp32 ("Where the gap actually is"; the LFM2 recipe's
+ * `fp32_router: true` in "The small-hardware end") in front of the per-token top-k of
+ * Figure 3.
+ *   logits[t][e] = sum_{i=0..d-1} x[t][i] * w_router[e][i]
+ * as one fp32 chain per logit in ascending i, each step adding the exact product of
+ * the two bf16 values with one rounding (an fmaf chain), so the logits, and the top-k
+ * taken on them exactly as moe_route does, are bit-reproducible. One block per 32
+ * tokens computes all E logits of its tokens on the fp32 SIMT pipes (the fixed order
+ * rules out tensor cores), stores them and routes the chunk.
+ *   x [T x d] bf16 in; w_router [E x d] bf16 in (one row per expert);
+ *   logits [T x E] fp32 out; ids [T x k] int32 out; w [T x k] fp32 out;
+ *   opts: see moe_route_options (aux_stats is ignored here) or NULL. */
+moe_status moe_router_route(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                            float *logits, int32_t *ids, float *w, const moe_route_options *opts,
+                            moe_stream stream);
+
+/* moe_forward with the router GEMM of moe_router_route in front: the first kernel
+ * computes the logits (written to `logits`, [T x E] fp32 out) and routes and counts
+ * the tokens in one pass; the rest is moe_forward. w_router [E x d] bf16 in; every
+ * other argument as in moe_forward. */
+moe_status moe_forward_router(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                              float *logits, const moe_bf16 *w_gu, const moe_bf16 *w_down,
+                              moe_bf16 *y, int training, const moe_route_options *opts, void *ws,
+                              size_t ws_bytes, moe_stream stream);
+
 /* Gradient of the load-balancing loss coeff * aux (see moe_route_options) with respect
  * to the router logits, ADDED into dlogits, with the assignment fractions f held
  * fixed (they count discrete choices):

@@ -64,6 +64,11 @@ _SIG = {
                                             _c_vp, _c_vp, _c_vp]),
     "moe_forward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_int,
                                    ctypes.POINTER(_RouteOptions), _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_router_route": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                        ctypes.POINTER(_RouteOptions), _c_vp]),
+    "moe_forward_router": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                          ctypes.c_int, ctypes.POINTER(_RouteOptions), _c_vp,
+                                          ctypes.c_size_t, _c_vp]),
     "moe_aux_loss_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
@@ -223,6 +228,25 @@ def route(logits: torch.Tensor, k: int, bias: torch.Tensor | None = None
     return ids, w
 
 
+def router_route(x: torch.Tensor, w_router: torch.Tensor, k: int,
+                 bias: torch.Tensor | None = None, logits: torch.Tensor | None = None
+                 ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """moe_router_route: fp32 logits = x w_router^T, then the route of moe_route.
+    x [T,d] bf16, w_router [E,d] bf16; returns (logits [T,E] fp32, ids, w)."""
+    _want(x, torch.bfloat16, "x")
+    _want(w_router, torch.bfloat16, "w_router")
+    T, d = x.shape
+    E = w_router.shape[0]
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    s = shape(T, d, E, k, 8)
+    _check(lib().moe_router_route(s, _p(x), _p(w_router), _p(logits), _p(ids), _p(w),
+                                  _options(bias, None), _stream()), "moe_router_route")
+    return logits, ids, w
+
+
 def dispatch(s: MoEShape, x: torch.Tensor, ids: torch.Tensor, ws: torch.Tensor | None = None) -> dict:
     """moe_dispatch: the stable counting sort of the assignments by expert."""
     _want(x, torch.bfloat16, "x")
@@ -312,6 +336,31 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w_gu: torch.Tensor, w_down: t
     return y, ws, s
 
 
+def forward_router(x: torch.Tensor, w_router: torch.Tensor, w_gu: torch.Tensor,
+                   w_down: torch.Tensor, k: int, training: bool = False,
+                   ws: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                   logits: torch.Tensor | None = None, bias: torch.Tensor | None = None,
+                   aux_stats: torch.Tensor | None = None
+                   ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor, MoEShape]:
+    """moe_forward_router: the block with the router GEMM in front.
+    Returns (y, logits [T,E] fp32, workspace, shape)."""
+    _want(x, torch.bfloat16, "x")
+    _want(w_router, torch.bfloat16, "w_router")
+    T, d = x.shape
+    E, _, f2 = w_gu.shape
+    s = shape(T, d, E, k, f2 // 2)
+    if ws is None:
+        ws = new_workspace(s, training, x.device)
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _check(lib().moe_forward_router(s, _p(x), _p(w_router), _p(logits), _p(w_gu), _p(w_down),
+                                    _p(y), int(bool(training)), _options(bias, aux_stats), _p(ws),
+                                    ws.numel(), _stream()), "moe_forward_router")
+    return y, logits, ws, s
+
+
 def aux_loss_backward(s: MoEShape, logits: torch.Tensor, counts: torch.Tensor, coeff: float,
                       dlogits: torch.Tensor) -> torch.Tensor:
     """moe_aux_loss_backward: adds coeff * d aux / d logits into dlogits (in place)."""
@@ -384,5 +433,6 @@ def launch_count() -> int:
 
 __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
-           "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward", "combine", "forward", "backward", "check_device_status", "debug_gate_up_withheld",
-           "profile_start", "profile_stop", "launch_count", "LIB_PATH"]
+           "router_route", "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward",
+           "combine", "forward", "forward_router", "backward", "check_device_status",
+           "debug_gate_up_withheld", "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

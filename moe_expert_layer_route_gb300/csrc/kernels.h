@@ -23,6 +23,12 @@ cudaError_t note_launch(const char *name, cudaStream_t st);
 cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, float *w,
                          int32_t *rank, int32_t *hist, float *prob_part, int T, int E, int k,
                          bool with_count, cudaStream_t st);
+// router.cu: logits = x W_r^T (fp32) and the route of launch_route from them; status
+// (may be null) records a staging load that timed out
+cudaError_t launch_router_route(const void *x, const void *w_r, const float *bias, float *logits,
+                                int32_t *ids, float *w, int32_t *rank, int32_t *hist,
+                                float *prob_part, int *status, int T, int d, int E, int k,
+                                bool with_count, cudaStream_t st);
 cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,
                             float *dlogits, int T, int E, int k, cudaStream_t st);
 cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,

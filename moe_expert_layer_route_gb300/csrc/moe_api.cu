@@ -285,16 +285,26 @@ moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int
   return MOE_OK;
 }
 
-moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
-                       const moe_bf16 *w_down, moe_bf16 *y, int training,
-                       const moe_route_options *opts, void *ws, size_t ws_bytes,
-                       moe_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward from router logits in memory (w_router null) or from the router GEMM
+// (w_router set: logits is then written).
+moe_status forward_impl(moe_shape s, const moe_bf16 *x, const float *logits_in,
+                        const moe_bf16 *w_router, float *logits_out, const moe_bf16 *w_gu,
+                        const moe_bf16 *w_down, moe_bf16 *y, int training,
+                        const moe_route_options *opts, void *ws, size_t ws_bytes,
+                        moe_stream stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(check_ptrs(w_gu, w_down, ws));
   const float *bias = opts ? opts->selection_bias : nullptr;
   float *aux = opts ? opts->aux_stats : nullptr;
   if ((bias && !aligned16(bias)) || (aux && !aligned16(aux))) return MOE_ERR_ALIGNMENT;
-  if (s.T > 0) MOE_TRY(check_ptrs(x, logits, y));
+  if (s.T > 0) {
+    MOE_TRY(check_ptrs(x, y));
+    MOE_TRY(w_router ? check_ptrs(w_router, logits_out) : check_ptrs(logits_in));
+  }
   const FwdLayout L = fwd_layout(s, training);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_TRY(check_device());
@@ -310,7 +320,11 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   void *gu = training ? at<void>(ws, L.gu) : nullptr;
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   float *prob_part = aux ? at<float>(ws, L.prob_part) : nullptr;
-  MOE_CUDA(launch_route(logits, bias, ids, w, rank, hist, prob_part, T, E, k, true, st));
+  if (w_router)
+    MOE_CUDA(launch_router_route(x, w_router, bias, logits_out, ids, w, rank, hist, prob_part,
+                                 status, T, d, E, k, true, st));
+  else
+    MOE_CUDA(launch_route(logits_in, bias, ids, w, rank, hist, prob_part, T, E, k, true, st));
   int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
   MOE_CUDA(launch_scan(hist, T, E, k, counts, at<int32_t>(ws, L.offsets), padded, tiles, pstart,
                        pexp, prob_part, aux, st));
@@ -321,6 +335,42 @@ moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, cons
   MOE_CUDA(gemm_gate_up(p, xp, w_gu, h, gu, d, f, status, st));
   MOE_CUDA(gemm_down(p, h, w_down, o, d, f, status, st));
   MOE_CUDA(launch_combine(o, w, row_of, y, T, d, k, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(moe_shape s, const moe_bf16 *x, const float *logits, const moe_bf16 *w_gu,
+                       const moe_bf16 *w_down, moe_bf16 *y, int training,
+                       const moe_route_options *opts, void *ws, size_t ws_bytes,
+                       moe_stream stream) {
+  return forward_impl(s, x, logits, nullptr, nullptr, w_gu, w_down, y, training, opts, ws,
+                      ws_bytes, stream);
+}
+
+moe_status moe_forward_router(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                              float *logits, const moe_bf16 *w_gu, const moe_bf16 *w_down,
+                              moe_bf16 *y, int training, const moe_route_options *opts, void *ws,
+                              size_t ws_bytes, moe_stream stream) {
+  if (s.T > 0 && !w_router) return MOE_ERR_INVALID_ARG;
+  return forward_impl(s, x, nullptr, w_router, logits, w_gu, w_down, y, training, opts, ws,
+                      ws_bytes, stream);
+}
+
+moe_status moe_router_route(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                            float *logits, int32_t *ids, float *w, const moe_route_options *opts,
+                            moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  const float *bias = opts ? opts->selection_bias : nullptr;
+  if (bias && !aligned16(bias)) return MOE_ERR_ALIGNMENT;
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(x, w_router, logits, ids, w));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_router_route(x, w_router, bias, logits, ids, w, nullptr, nullptr, nullptr,
+                               nullptr, (int)s.T, (int)s.d, (int)s.E, (int)s.k, false,
+                               static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

@@ -8,129 +8,17 @@
 // written by one thread and every sum runs in a fixed order, so results are
 // bit-reproducible without atomics ("The hard problems along the way" in "Halo:
 // Frontier-Lab Training for Everyone" credits an atomic-free routing backward).
-#include "kernels.h"
+#include "route_common.cuh"
 
 namespace moe {
 
-constexpr int kChunk = 32;        // tokens per histogram chunk (one per lane of a warp)
-constexpr int kMaxK = 16;
-constexpr int kMaxE = 256;
 constexpr int kVec = 4;           // 16-byte vectors each lane keeps in flight in the row copies
-
-// ---------------------------------------------------------------------------- route
-// One warp per token. Lane l holds logits l, l+32, ... (E <= 256, so <= 8 each).
-// k rounds of a warp arg-max of the score under the order (score descending, index
-// ascending); lane j keeps slot j. The score is the logit, or logit + bias[e] in fp32
-// with a selection bias. Weights: softmax over the k chosen unbiased logits in fp32.
-// With prob (aux statistics) the lane also returns the full softmax over all E
-// unbiased logits for its experts.
-__device__ __forceinline__ void route_one_token(const float *__restrict__ row,
-                                                const float *__restrict__ bias, int E, int k,
-                                                int lane, int &slot_id, float &slot_w,
-                                                float (*prob)[8]) {
-  float v[8], sc[8];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int e = lane + 32 * q;
-    v[q] = (e < E) ? __ldg(row + e) : 0.f;
-    sc[q] = (e < E && bias) ? v[q] + __ldg(bias + e) : v[q];
-    if (e >= E) taken |= 1u << q;
-  }
-  const uint32_t valid = ~taken & 0xffu;
-  float my_l = 0.f;
-  int my_i = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.f;
-    int bi = 0x7fffffff;  // "none"
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (!((taken >> q) & 1u)) {
-        // candidates in ascending index: strict '>' keeps the lower index on ties
-        if (bi == 0x7fffffff || sc[q] > bv) {
-          bv = sc[q];
-          bi = lane + 32 * q;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const bool better = (oi != 0x7fffffff) &&
-                          (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (better) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    const bool mine = (bi & 31) == lane;
-    float lv = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (mine && (bi >> 5) == q) lv = v[q];
-    lv = __shfl_sync(0xffffffffu, lv, bi & 31);  // the chosen expert's unbiased logit
-    if (mine) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_l = lv;
-      my_i = bi;
-    }
-  }
-  float m = (lane < k) ? my_l : -INFINITY;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float z = (lane < k) ? expf(my_l - m) : 0.f;
-  float s = z;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  slot_id = my_i;
-  slot_w = z / s;
-  if (prob) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if ((valid >> q) & 1u) mx = fmaxf(mx, v[q]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float ex[8], sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      ex[q] = ((valid >> q) & 1u) ? expf(v[q] - mx) : 0.f;
-      sum += ex[q];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) (*prob)[q] = ex[q] / sum;
-  }
-}
-
-// Ballot count of one chunk of 32 tokens: for each expert, the number of tokens of
-// the chunk that chose it (hist[e][c]) and, for each (token, slot), the number of
-// earlier tokens of the chunk that chose the same expert (the stable local rank).
-__device__ __forceinline__ void count_chunk(const int32_t (*s_ids)[kMaxK], int c, int T, int E,
-                                            int k, int C, int warp, int nwarps, int lane,
-                                            int32_t *__restrict__ rank,
-                                            int32_t *__restrict__ hist) {
-  const int t = c * kChunk + lane;
-  const bool valid = t < T;
-  for (int e = warp; e < E; e += nwarps) {
-    int slot = -1;
-    if (valid) {
-      for (int j = 0; j < k; ++j)
-        if (s_ids[lane][j] == e) slot = j;
-    }
-    const uint32_t m = __ballot_sync(0xffffffffu, slot >= 0);
-    if (slot >= 0) rank[(int64_t)t * k + slot] = __popc(m & lanemask_lt());
-    if (lane == 0) hist[(int64_t)e * C + c] = __popc(m);
-  }
-}
 
 // Block c routes tokens [32c, 32c+32), one warp per token, and, when COUNT, also
 // writes the chunk histogram and local ranks for the dispatch. With prob_part it also
 // writes prob_part[e][c], the sum over the chunk's tokens (in token order) of the
 // softmax of all E logits, for the load-balancing statistics.
-template <bool COUNT>
+template <bool COUNT, int Q>
 __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ logits,
                                                      const float *__restrict__ bias,
                                                      int32_t *__restrict__ ids,
@@ -150,18 +38,19 @@ __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ l
         for (int e = lane; e < E; e += 32) s_prob[i][e] = 0.f;
       break;
     }
-    int sid;
-    float sw, pr[8];
-    route_one_token(logits + (int64_t)t * E, bias, E, k, lane, sid, sw, prob_part ? &pr : nullptr);
+    int sid[1];
+    float sw[1], pr[1][Q];
+    route_tokens<Q, 1, false>(logits + (int64_t)t * E, E, bias, E, k, lane, sid, sw,
+                              prob_part != nullptr, pr);
     if (lane < k) {
-      ids[(int64_t)t * k + lane] = sid;
-      w[(int64_t)t * k + lane] = sw;
-      s_ids[i][lane] = sid;
+      ids[(int64_t)t * k + lane] = sid[0];
+      w[(int64_t)t * k + lane] = sw[0];
+      s_ids[i][lane] = sid[0];
     }
     if (prob_part) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (lane + 32 * q < E) s_prob[i][lane + 32 * q] = pr[q];
+      for (int q = 0; q < Q; ++q)
+        if (lane + 32 * q < E) s_prob[i][lane + 32 * q] = pr[0][q];
     }
   }
   if (COUNT || prob_part) __syncthreads();
@@ -578,16 +467,23 @@ cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, f
                          bool with_count, cudaStream_t st) {
   const int C = ceil_div(T, kChunk);
   if (C == 0) return cudaSuccess;
-  if (with_count) {
-    launch_begin(st);
-    route_kernel<true><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist, prob_part, T, E, k,
-                                           C);
-    return note_launch("route_count", st);
-  }
-  launch_begin(st);
-  route_kernel<false><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist, prob_part, T, E, k,
-                                          C);
-  return note_launch("route", st);
+  // Q = logits per lane: the smallest of 1, 2, 4, 8 with E <= 32 Q
+#define MOE_ROUTE(Q)                                                                        \
+  do {                                                                                     \
+    launch_begin(st);                                                                      \
+    if (with_count)                                                                        \
+      route_kernel<true, Q><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,          \
+                                                prob_part, T, E, k, C);                    \
+    else                                                                                   \
+      route_kernel<false, Q><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,         \
+                                                 prob_part, T, E, k, C);                   \
+    return note_launch(with_count ? "route_count" : "route", st);                         \
+  } while (0)
+  if (E <= 32) MOE_ROUTE(1);
+  if (E <= 64) MOE_ROUTE(2);
+  if (E <= 128) MOE_ROUTE(4);
+  MOE_ROUTE(8);
+#undef MOE_ROUTE
 }
 
 cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,

@@ -104,6 +104,14 @@ def test_pointer_and_workspace_validation(moe):
                           scratch, None) == -3
     assert L.moe_combine(s, good, good, good, null, None) == -1
     assert L.moe_route(s, good, good, odd, None, None) == -3
+    assert L.moe_router_route(s, good, odd, good, good, good, None, None) == -3
+    assert L.moe_router_route(s, good, null, good, good, good, None, None) == -1
+    assert L.moe_forward_router(s, good, null, good, good, good, good, 1, None, good, need,
+                                None) == -1
+    assert L.moe_forward_router(s, good, good, odd, good, good, good, 1, None, good, need,
+                                None) == -3
+    assert L.moe_forward_router(s, good, good, good, good, good, good, 1, None, good, need - 1,
+                                None) == -4
 
 
 def test_views_follow_the_layout(moe):
