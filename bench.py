@@ -103,11 +103,26 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
+# fp32 SIMT peak for the router GEMM (plain ALU arithmetic, no tensor cores): 152 SMs x
+# 128 fp32 lanes x 2 FLOP per fma x 2.07 GHz maximum SM clock
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def router_splits(T: int, d: int, E: int) -> int:
+    cells = -(-d // 256) * -(-E // 32)
+    return max(1, min(-(-304 // cells), -(-T // 32)))
+
+
 def kernel_work(wl: workloads.Workload) -> dict:
-    """Algorithmic work of one launch of each kernel: ('flop'|'byte', amount)."""
+    """Algorithmic work of one launch of each kernel: ('flop'|'alu_flop'|'byte', amount)."""
     T, d, E, k, f, A = wl.T, wl.d, wl.E, wl.k, wl.f, wl.A
     C = (T + 31) // 32
     return {
+        "router_route_count": ("alu_flop", 2 * T * E * d),
+        "router_dx": ("alu_flop", 2 * T * E * d),
+        "router_dw": ("alu_flop", 2 * T * E * d),
+        # the library's token splits of dW_r: about 2 x 152 blocks of 256 columns x 32 experts
+        "router_dw_reduce": ("byte", (router_splits(T, d, E) + 1) * E * d * 4),
         "gemm_gate_up_swiglu": ("flop", 4 * A * d * f),
         "gemm_down": ("flop", 2 * A * d * f),
         "gemm_dgrad_h_swiglu_bwd": ("flop", 2 * A * d * f),
@@ -189,17 +204,21 @@ def oracle_step(oracle, inp_np: dict, n_tok: int, k: int) -> float:
     """Forward (+ backward when the workload has one) of the oracle on the first n_tok
     tokens; returns seconds."""
     t0 = time.perf_counter()
-    ref = oracle.forward(inp_np["x"][:n_tok], inp_np["logits"][:n_tok], inp_np["w_gu"],
-                         inp_np["w_down"], k)
+    if inp_np.get("w_router") is not None:  # the fp32 router GEMM in front
+        logits = oracle.router_logits(inp_np["x"][:n_tok], inp_np["w_router"])
+    else:
+        logits = inp_np["logits"][:n_tok]
+    ref = oracle.forward(inp_np["x"][:n_tok], logits, inp_np["w_gu"], inp_np["w_down"], k)
     if inp_np["dy"] is not None:
         oracle.backward(inp_np["dy"][:n_tok], ref, inp_np["w_gu"], inp_np["w_down"])
     return time.perf_counter() - t0
 
 
-def oracle_inputs(inp: workloads.Inputs, backward: bool) -> dict:
+def oracle_inputs(inp: workloads.Inputs, backward: bool, w_router=None) -> dict:
     return {"x": inp.x.float().numpy(), "logits": inp.logits.numpy(),
             "w_gu": inp.w_gu.float().numpy(), "w_down": inp.w_down.float().numpy(),
-            "dy": inp.dy.float().numpy() if backward else None}
+            "dy": inp.dy.float().numpy() if backward else None,
+            "w_router": None if w_router is None else w_router.float().numpy()}
 
 
 def cpu_threads() -> int:
@@ -213,10 +232,10 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, inp, seconds: float) -> dict:
+def cpu_baseline(wl, inp, seconds: float, w_router=None) -> dict:
     """The oracle as it stands on a bounded token sample sized to about `seconds`."""
     import oracle
-    inp_np = oracle_inputs(inp, wl.backward)
+    inp_np = oracle_inputs(inp, wl.backward, w_router)
     n = 16
     t = oracle_step(oracle, inp_np, n, wl.k)
     while t < seconds / 4 and n < wl.T:
@@ -224,7 +243,8 @@ def cpu_baseline(wl, inp, seconds: float) -> dict:
         t = oracle_step(oracle, inp_np, n, wl.k)
     return {"value": n / t, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"first {n} of {wl.T} tokens of the {wl.name} workload, "
-                      f"{'forward+backward' if wl.backward else 'forward'} in fp64 numpy, "
+                      f"{'forward+backward' if wl.backward else 'forward'}"
+                      f"{' with the router GEMM' if w_router is not None else ''} in fp64 numpy, "
                       f"{t:.1f} s"}
 
 
@@ -254,6 +274,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     wl = workload_of(args)
     inp = workloads.make_inputs(wl, with_dy=True)
     x, logits = inp.x.to(dev), inp.logits.to(dev)
+    w_router = workloads.make_router_weight(wl).to(dev) if args.router_gemm else None
+    dw_router = torch.empty(w_router.shape, dtype=torch.float32, device=dev) \
+        if w_router is not None else None
     w_gu, w_down, dy = inp.w_gu.to(dev), inp.w_down.to(dev), inp.dy.to(dev)
     s = moe.shape(wl.T, wl.d, wl.E, wl.k, wl.f)
     ws = moe.new_workspace(s, wl.backward, dev)
@@ -265,15 +288,23 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     sel_bias = torch.from_numpy(workloads.zipf_bias(wl.E)).to(dev) if args.selection_bias else None
     aux = torch.empty(2 * wl.E + 1, dtype=torch.float32, device=dev) if args.aux_loss else None
     views = None
+    r_scratch = torch.empty(max(16, moe.lib().moe_router_backward_scratch_size(s)),
+                            dtype=torch.uint8, device=dev) if w_router is not None else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y,
-                    bias=sel_bias, aux_stats=aux)
+        if w_router is not None:  # logits computed from x by the router GEMM
+            moe.forward_router(x, w_router, w_gu, w_down, wl.k, training=wl.backward, ws=ws,
+                               y=y, logits=logits, bias=sel_bias, aux_stats=aux)
+        else:
+            moe.forward(x, logits, w_gu, w_down, wl.k, training=wl.backward, ws=ws, y=y,
+                        bias=sel_bias, aux_stats=aux)
         if wl.backward:
             moe.backward(s, dy, w_gu, w_down, ws, scratch, out=grads, dlogits=dlogits)
             if aux is not None:
                 moe.aux_loss_backward(s, logits, views["counts"], 0.01, dlogits)
+            if w_router is not None and dlogits is not None:  # through the router GEMM
+                moe.router_backward(s, x, w_router, dlogits, grads[0], dw_router, r_scratch)
 
     views = moe.workspace_views(s, wl.backward, ws)
 
@@ -290,7 +321,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
     launches0 = moe.launch_count()
-    moe.profile_start(capacity=K * 16)
+    moe.profile_start(capacity=K * 24)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clk:
@@ -301,7 +332,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
             ends[i].record()
         torch.cuda.synchronize()
     barrier(world)
-    records = moe.profile_stop(capacity=K * 16)
+    records = moe.profile_stop(capacity=K * 24)
     launches = moe.launch_count() - launches0
     moe.check_device_status(ws)
     moe.check_device_status(scratch)
@@ -325,6 +356,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
             if kind == "flop":
                 entry.update(achieved=amount / (mean * 1e-3) / 1e12, unit="TFLOP/s",
                              frac=amount / (mean * 1e-3) / 1e12 / pk["bf16_tflops_sustained"])
+            elif kind == "alu_flop":
+                entry.update(achieved=amount / (mean * 1e-3) / 1e12, unit="TFLOP/s fp32",
+                             frac=amount / (mean * 1e-3) / 1e12 / FP32_ALU_TFLOPS)
             else:
                 entry.update(achieved=amount / (mean * 1e-3) / 1e9, unit="GB/s",
                              frac=amount / (mean * 1e-3) / 1e9 / pk["hbm_gbs"])
@@ -369,7 +403,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
 
         def e2e_step():
             x.copy_(hx, non_blocking=True)
-            logits.copy_(hl, non_blocking=True)
+            if w_router is None:
+                logits.copy_(hl, non_blocking=True)
             if wl.backward:
                 dy.copy_(hdy, non_blocking=True)
             step()
@@ -391,7 +426,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) * 1e3 / ke
         e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
-        h2d = hx.numel() * 2 + hl.numel() * 4 + (hdy.numel() * 2 if wl.backward else 0)
+        h2d = hx.numel() * 2 + (hl.numel() * 4 if w_router is None else 0) + \
+            (hdy.numel() * 2 if wl.backward else 0)
         d2h = hy.numel() * 2 + (hdx.numel() * 2 if wl.backward else 0)
         e2e = {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
@@ -405,7 +441,10 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                    "f": wl.f, "seed": wl.seed,
                    "passes": ("forward+backward" if wl.backward else "forward")
+                   + (" + fp32 router GEMM (logits from x)" if args.router_gemm else "")
                    + (" + router-logit gradient" if router_grad and wl.backward else "")
+                   + (" + router GEMM gradient (dW_r, dX)" if args.router_gemm and router_grad
+                      and wl.backward else "")
                    + (" + selection bias (Zipf)" if args.selection_bias else "")
                    + (" + load-balancing statistics and gradient" if args.aux_loss else ""),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -421,7 +460,8 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "e2e": e2e,
     }
     if not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds,
+                                           None if w_router is None else w_router.cpu())
     return out
 
 
@@ -433,7 +473,8 @@ def run_reference(args, rank, world) -> dict | None:
     import oracle
     wl = workload_of(args)
     inp = workloads.make_inputs(wl, with_dy=wl.backward)
-    inp_np = oracle_inputs(inp, wl.backward)
+    inp_np = oracle_inputs(inp, wl.backward,
+                           workloads.make_router_weight(wl) if args.router_gemm else None)
     budget = args.reference_seconds / max(1, args.steps + args.warmup)
     n = 4
     t = oracle_step(oracle, inp_np, n, wl.k)
@@ -447,7 +488,8 @@ def run_reference(args, rank, world) -> dict | None:
     value = n / sec
     cores = cpu_threads()
     sample = (f"first {n} of {wl.T} tokens of the {wl.name} workload per step, "
-              f"{'forward+backward' if wl.backward else 'forward'} in fp64 numpy")
+              f"{'forward+backward' if wl.backward else 'forward'}"
+              f"{' with the router GEMM' if args.router_gemm else ''} in fp64 numpy")
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
@@ -455,7 +497,8 @@ def run_reference(args, rank, world) -> dict | None:
         "impl": "reference",
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                    "f": wl.f, "seed": wl.seed,
-                   "passes": "forward+backward" if wl.backward else "forward"},
+                   "passes": ("forward+backward" if wl.backward else "forward")
+                   + (" + fp32 router GEMM (logits from x)" if args.router_gemm else "")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -475,6 +518,8 @@ def main(argv=None) -> int:
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--router-grad", action="store_true",
                     help="also compute the router-logit gradient in the backward")
+    ap.add_argument("--router-gemm", action="store_true",
+                    help="compute the fp32 router logits from x in the step (fused with top-k)")
     ap.add_argument("--selection-bias", action="store_true",
                     help="route on logits + a per-expert selection bias (Zipf ranks)")
     ap.add_argument("--aux-loss", action="store_true",

@@ -217,6 +217,24 @@ moe_status moe_forward_router(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_
                               moe_bf16 *y, int training, const moe_route_options *opts, void *ws,
                               size_t ws_bytes, moe_stream stream);
 
+/* Bytes of scratch moe_router_backward needs (token-split partial sums of dW_r). */
+size_t moe_router_backward_scratch_size(moe_shape s);
+
+/* Gradient through the router GEMM of moe_router_route / moe_forward_router, for a
+ * router-logit gradient dlogits (for instance moe_backward's, plus
+ * moe_aux_loss_backward's):
+ *   dw_router[e][i] = sum_t dlogits[t][e] * x[t][i]          (fp32, the fp32 router)
+ *   dx[t][i] = bf16( dx[t][i] + sum_e dlogits[t][e] * w_router[e][i] )
+ * so that dx, holding moe_backward's dX on entry, holds the whole input gradient on
+ * return (one more bf16 rounding of dx). fp32 sums on the SIMT pipes; dW_r sums token
+ * splits in order and then adds the splits in order (no atomics, bit-reproducible).
+ *   x [T x d] bf16 in; w_router [E x d] bf16 in; dlogits [T x E] fp32 in;
+ *   dx [T x d] bf16 in/out; dw_router [E x d] fp32 out;
+ *   scratch: at least moe_router_backward_scratch_size(s) bytes. */
+moe_status moe_router_backward(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                               const float *dlogits, moe_bf16 *dx, float *dw_router,
+                               void *scratch, size_t scratch_bytes, moe_stream stream);
+
 /* Gradient of the load-balancing loss coeff * aux (see moe_route_options) with respect
  * to the router logits, ADDED into dlogits, with the assignment fractions f held
  * fixed (they count discrete choices):

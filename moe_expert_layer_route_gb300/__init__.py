@@ -69,6 +69,9 @@ _SIG = {
     "moe_forward_router": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                           ctypes.c_int, ctypes.POINTER(_RouteOptions), _c_vp,
                                           ctypes.c_size_t, _c_vp]),
+    "moe_router_backward_scratch_size": (ctypes.c_size_t, [MoEShape]),
+    "moe_router_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                           ctypes.c_size_t, _c_vp]),
     "moe_aux_loss_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
@@ -361,6 +364,25 @@ def forward_router(x: torch.Tensor, w_router: torch.Tensor, w_gu: torch.Tensor,
     return y, logits, ws, s
 
 
+def router_backward(s: MoEShape, x: torch.Tensor, w_router: torch.Tensor,
+                    dlogits: torch.Tensor, dx: torch.Tensor, dw_router: torch.Tensor | None = None,
+                    scratch: torch.Tensor | None = None) -> torch.Tensor:
+    """moe_router_backward: adds dlogits w_router into dx (in place); returns dW_r [E,d] fp32."""
+    _want(x, torch.bfloat16, "x")
+    _want(w_router, torch.bfloat16, "w_router")
+    _want(dlogits, torch.float32, "dlogits")
+    _want(dx, torch.bfloat16, "dx")
+    if dw_router is None:
+        dw_router = torch.empty(w_router.shape, dtype=torch.float32, device=x.device)
+    need = int(lib().moe_router_backward_scratch_size(s))
+    if scratch is None or scratch.numel() < need:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_router_backward(s, _p(x), _p(w_router), _p(dlogits), _p(dx), _p(dw_router),
+                                     _p(scratch), scratch.numel(), _stream()),
+           "moe_router_backward")
+    return dw_router
+
+
 def aux_loss_backward(s: MoEShape, logits: torch.Tensor, counts: torch.Tensor, coeff: float,
                       dlogits: torch.Tensor) -> torch.Tensor:
     """moe_aux_loss_backward: adds coeff * d aux / d logits into dlogits (in place)."""
@@ -434,5 +456,5 @@ def launch_count() -> int:
 __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_size",
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
            "router_route", "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward",
-           "combine", "forward", "forward_router", "backward", "check_device_status",
+           "combine", "forward", "forward_router", "backward", "router_backward", "check_device_status",
            "debug_gate_up_withheld", "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

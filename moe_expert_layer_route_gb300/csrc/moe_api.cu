@@ -411,6 +411,31 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   return MOE_OK;
 }
 
+size_t moe_router_backward_scratch_size(moe_shape s) {
+  if (check_shape(s) != MOE_OK) return 0;
+  const int splits = router_dw_splits((int)s.T, (int)s.d, (int)s.E);
+  return splits > 1 ? (size_t)splits * s.E * s.d * sizeof(float) : 16;
+}
+
+moe_status moe_router_backward(moe_shape s, const moe_bf16 *x, const moe_bf16 *w_router,
+                               const float *dlogits, moe_bf16 *dx, float *dw_router,
+                               void *scratch, size_t scratch_bytes, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(w_router, dw_router, scratch));
+  if (s.T > 0) MOE_TRY(check_ptrs(x, dlogits, dx));
+  if (scratch_bytes < moe_router_backward_scratch_size(s)) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(dw_router, 0, (size_t)s.E * s.d * sizeof(float), st));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_router_backward(x, w_router, dlogits, dx, dw_router,
+                                  static_cast<float *>(scratch), (int)s.T, (int)s.d, (int)s.E,
+                                  st));
+  return MOE_OK;
+}
+
 moe_status moe_aux_loss_backward(moe_shape s, const float *logits, const int32_t *counts,
                                  float coeff, float *dlogits, moe_stream stream) {
   MOE_TRY(check_shape(s));

@@ -439,6 +439,149 @@ cudaError_t launch_router_cfg(const void *x, const void *w_r, const float *bias,
 #undef MOE_ROUTER
 }
 
+// ------------------------------------------------------------------- router backward
+// The gradient through logits = x W_r^T for a given dlogits [T][E] (fp32):
+//   dW_r[e][i] = sum_t dlogits[t][e] x[t][i]       dX[t][i] += sum_e dlogits[t][e] W_r[e][i]
+// Both in fp32 on the SIMT pipes (dlogits is fp32; bf16 operands are widened exactly).
+// A thread owns 4 rows x 8 columns (one 16-byte bf16 vector of the wide operand); per
+// step of the reduction it loads 4 fp32 values (the same for the whole warp) and 8 bf16.
+
+constexpr int kRbCols = 256;     // columns of d per block (8 per lane)
+constexpr int kRbRows = 32;      // tokens (dX) or experts (dW) per block: 4 per warp
+
+// dX: block (token chunk, column block). dl and W_r staged 64 experts at a time.
+__global__ void __launch_bounds__(256) router_dx_kernel(const float *__restrict__ dl,
+                                                        const uint4 *__restrict__ w_r,
+                                                        uint4 *__restrict__ dx, int T, int d,
+                                                        int E) {
+  constexpr int EB = 64;
+  __shared__ __align__(16) float s_dl[EB][kRbRows + 4];    // [e][token], padded rows
+  __shared__ __align__(16) uint4 s_w[EB][kRbCols / 8];     // [e][8-column vector]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kRbRows, c0 = blockIdx.y * kRbCols;
+  const int nvr = d >> 3, v = (c0 >> 3) + lane;            // this lane's column vector
+  float acc[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
+  for (int e0 = 0; e0 < E; e0 += EB) {
+    const int ne = min(EB, E - e0);
+    __syncthreads();  // the previous tiles are consumed
+    for (int idx = threadIdx.x; idx < EB * kRbRows; idx += 256) {
+      const int t = idx / EB, e = idx % EB;  // consecutive threads: consecutive experts
+      s_dl[e][t] = (e < ne && t0 + t < T) ? dl[(int64_t)(t0 + t) * E + e0 + e] : 0.f;
+    }
+    for (int idx = threadIdx.x; idx < EB * (kRbCols / 8); idx += 256) {
+      const int e = idx / (kRbCols / 8), c = idx % (kRbCols / 8);
+      const int vv = (c0 >> 3) + c;
+      s_w[e][c] = (e < ne && vv < nvr) ? ldg_nc(w_r + (int64_t)(e0 + e) * nvr + vv)
+                                       : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    for (int e = 0; e < ne; ++e) {
+      const float4 g = *reinterpret_cast<const float4 *>(&s_dl[e][4 * warp]);
+      float wv[8];
+      unpack8(s_w[e][lane], wv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[0][j] = fmaf(g.x, wv[j], acc[0][j]);
+        acc[1][j] = fmaf(g.y, wv[j], acc[1][j]);
+        acc[2][j] = fmaf(g.z, wv[j], acc[2][j]);
+        acc[3][j] = fmaf(g.w, wv[j], acc[3][j]);
+      }
+    }
+  }
+  if (v >= nvr) return;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int t = t0 + 4 * warp + a;
+    if (t >= T) break;
+    uint4 *p = dx + (int64_t)t * nvr + v;
+    float f[8];
+    unpack8(*p, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] += acc[a][j];
+    *p = pack8(f);
+  }
+}
+
+// dW partials: block (column block, expert block, token split). Token tiles of 32;
+// each split sums its tokens in order into part[split][e][i] (or straight into dW when
+// there is one split).
+__global__ void __launch_bounds__(256) router_dw_kernel(const float *__restrict__ dl,
+                                                        const uint4 *__restrict__ x,
+                                                        float *__restrict__ part, int T, int d,
+                                                        int E, int split_tokens) {
+  constexpr int TB = 32;
+  __shared__ __align__(16) float s_dl[TB][kRbRows];        // [token][expert]
+  __shared__ __align__(16) uint4 s_x[TB][kRbCols / 8];     // [token][8-column vector]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * kRbCols, e0 = blockIdx.y * kRbRows;
+  const int ts = blockIdx.z;
+  const int tbeg = ts * split_tokens, tend = min(T, tbeg + split_tokens);
+  const int nvr = d >> 3, v = (c0 >> 3) + lane;
+  float acc[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
+  for (int t0 = tbeg; t0 < tend; t0 += TB) {
+    const int nt = min(TB, tend - t0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < TB * kRbRows; idx += 256) {
+      const int t = idx / kRbRows, e = idx % kRbRows;
+      s_dl[t][e] = (t < nt && e0 + e < E) ? dl[(int64_t)(t0 + t) * E + e0 + e] : 0.f;
+    }
+    for (int idx = threadIdx.x; idx < TB * (kRbCols / 8); idx += 256) {
+      const int t = idx / (kRbCols / 8), c = idx % (kRbCols / 8);
+      const int vv = (c0 >> 3) + c;
+      s_x[t][c] = (t < nt && vv < nvr) ? ldg_nc(x + (int64_t)(t0 + t) * nvr + vv)
+                                       : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    for (int t = 0; t < nt; ++t) {
+      const float4 g = *reinterpret_cast<const float4 *>(&s_dl[t][4 * warp]);
+      float xv[8];
+      unpack8(s_x[t][lane], xv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[0][j] = fmaf(g.x, xv[j], acc[0][j]);
+        acc[1][j] = fmaf(g.y, xv[j], acc[1][j]);
+        acc[2][j] = fmaf(g.z, xv[j], acc[2][j]);
+        acc[3][j] = fmaf(g.w, xv[j], acc[3][j]);
+      }
+    }
+  }
+  if (v >= nvr) return;
+  float *out = part + (int64_t)ts * E * d;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int e = e0 + 4 * warp + a;
+    if (e >= E) break;
+    float4 *p = reinterpret_cast<float4 *>(out + (int64_t)e * d + 8 * (int64_t)v);
+    p[0] = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    p[1] = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+  }
+}
+
+// dW = sum of the splits' partials, in split order.
+__global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float4 *__restrict__ part,
+                                                               float4 *__restrict__ dw,
+                                                               int64_t n4, int splits) {
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
+    float4 s = part[i];
+    for (int p = 1; p < splits; ++p) {
+      const float4 q = part[(int64_t)p * n4 + i];
+      s.x += q.x;
+      s.y += q.y;
+      s.z += q.z;
+      s.w += q.w;
+    }
+    dw[i] = s;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_router_route(const void *x, const void *w_r, const float *bias, float *logits,
@@ -452,6 +595,44 @@ cudaError_t launch_router_route(const void *x, const void *w_r, const float *bia
                                    d, E, k, C, st);
   return launch_router_cfg<false>(x, w_r, bias, logits, ids, w, rank, hist, prob_part, status, T,
                                   d, E, k, C, st);
+}
+
+// The token splits of dW_r: about two waves of blocks on the 152 SMs of a GB300, fixed
+// by the shape alone so that the scratch size and the order of the sums are the same on
+// every machine.
+int router_dw_splits(int T, int d, int E) {
+  const int cells = ((d + kRbCols - 1) / kRbCols) * ((E + kRbRows - 1) / kRbRows);
+  const int chunks = (T + 31) / 32;
+  const int splits = (2 * 152 + cells - 1) / cells;
+  return max(1, min(splits, chunks));
+}
+
+cudaError_t launch_router_backward(const void *x, const void *w_r, const float *dlogits, void *dx,
+                                   float *dw, float *part, int T, int d, int E, cudaStream_t st) {
+  const dim3 bdx((T + kRbRows - 1) / kRbRows, (d + kRbCols - 1) / kRbCols);
+  if (T > 0) {
+    launch_begin(st);
+    router_dx_kernel<<<bdx, 256, 0, st>>>(dlogits, static_cast<const uint4 *>(w_r),
+                                          static_cast<uint4 *>(dx), T, d, E);
+    cudaError_t e = note_launch("router_dx", st);
+    if (e != cudaSuccess) return e;
+  }
+  const int splits = router_dw_splits(T, d, E);
+  const int chunks = max(1, (T + 31) / 32);
+  const int split_tokens = ((chunks + splits - 1) / splits) * 32;
+  const int nsplit = T > 0 ? (T + split_tokens - 1) / split_tokens : 1;  // <= splits
+  const dim3 bdw((d + kRbCols - 1) / kRbCols, (E + kRbRows - 1) / kRbRows, nsplit);
+  launch_begin(st);
+  router_dw_kernel<<<bdw, 256, 0, st>>>(dlogits, static_cast<const uint4 *>(x),
+                                        nsplit == 1 ? dw : part, T, d, E, split_tokens);
+  cudaError_t e = note_launch("router_dw", st);
+  if (e != cudaSuccess || nsplit == 1) return e;
+  const int64_t n4 = (int64_t)E * d / 4;
+  const int64_t blocks = (n4 + 255) / 256, cap = 4 * (int64_t)num_sms();
+  launch_begin(st);
+  router_dw_reduce_kernel<<<(int)(blocks < cap ? blocks : cap), 256, 0, st>>>(
+      reinterpret_cast<const float4 *>(part), reinterpret_cast<float4 *>(dw), n4, nsplit);
+  return note_launch("router_dw_reduce", st);
 }
 
 }  // namespace moe

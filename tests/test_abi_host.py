@@ -112,6 +112,21 @@ def test_pointer_and_workspace_validation(moe):
                                 None) == -3
     assert L.moe_forward_router(s, good, good, good, good, good, good, 1, None, good, need - 1,
                                 None) == -4
+    rneed = L.moe_router_backward_scratch_size(s)
+    assert rneed >= 16
+    assert L.moe_router_backward(s, good, good, good, good, good, good, rneed - 1, None) == -4
+    assert L.moe_router_backward(s, good, good, good, good, odd, good, rneed, None) == -3
+    assert L.moe_router_backward(s, good, null, good, good, good, good, rneed, None) == -1
+
+
+def test_router_backward_scratch_is_fixed_by_the_shape(moe):
+    L = moe.lib()
+    # 2880 columns in 12 blocks of 256, 32 experts in one block: ceil(304 / 12) = 26
+    # token splits of 160 tokens, E * d floats each
+    assert L.moe_router_backward_scratch_size(moe.shape(4096, 2880, 32, 4, 2880)) == \
+        26 * 32 * 2880 * 4
+    assert L.moe_router_backward_scratch_size(moe.shape(32, 64, 8, 2, 64)) == 16  # one split
+    assert L.moe_router_backward_scratch_size(moe.shape(16, 60, 8, 2, 64)) == 0   # bad shape
 
 
 def test_views_follow_the_layout(moe):

@@ -32,6 +32,7 @@ def _rank_main(rank: int, world: int, port: int, q) -> None:
             steps, warmup, workload = 1, 3, "tiny"
             reference_seconds = 1.0
             tokens = experts = None
+            router_gemm = False
         ref = bench.run_reference(A, r, w) if r != 0 else "skipped"
         q.put((r, w, lr, mx, sm, ref))
     finally:

@@ -42,4 +42,6 @@ def test_withheld_loads_time_out_and_the_context_survives(moe, T, E):
     h1, _, o1 = moe.expert_ffn(s, disp["xp"], disp["counts"], w_gu, w_down, ws=ws)
     torch.cuda.synchronize()
     moe.check_device_status(ws)
-    assert torch.equal(h0, h1) and torch.equal(o0, o1)
+    # rows at and past padded_offsets[E] belong to no expert and are never written
+    P = int(disp["padded_offsets"][-1])
+    assert torch.equal(h0[:P], h1[:P]) and torch.equal(o0[:P], o1[:P])
