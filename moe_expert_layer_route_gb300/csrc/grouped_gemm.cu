@@ -91,6 +91,7 @@ struct Args {
 // feed the MMA but nothing is stored).
 struct Tile {
   int e, m0, n0, kt, kr0;
+  int klast;  // 16-row K slices of the last k-block that hold rows (WGRAD; else 4)
   bool valid;
 };
 
@@ -106,6 +107,7 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
   constexpr int kMTile = Cfg<PAIR>::kMTile;
   Tile t;
   t.valid = true;
+  t.klast = BK / 16;
   if (KIND == WGRAD) {
     const int per = a.m_tiles * a.n_tiles;
     t.e = tile / per;
@@ -114,6 +116,9 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
     t.n0 = (r % a.n_tiles) * BN;
     t.kr0 = a.padded[t.e];
     t.kt = (a.counts[t.e] + BK - 1) / BK;  // k-blocks holding the expert's rows
+    // the last k-block's rows past the count are zero padding: its MMAs stop at the
+    // last 16-row slice that holds a row
+    t.klast = (a.counts[t.e] - (t.kt - 1) * BK + 15) / 16;
     return t;
   }
   // ragged M: "units" are 128-row tiles (single) or pairs of them (pair mode);
@@ -540,12 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t a_addr = smem_base + s * kStageBytes;
             const uint32_t b_addr = a_addr + kABytes;
+            const int nk = (kb == t.kt - 1) ? t.klast : BK / 16;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
-              const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
-              if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
-              else tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+              if (kk < nk) {
+                const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
+                const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
+                if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+                else tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+              }
             }
             any = true;
             if (kPair) tc_commit_pair(&empty_bar[s]);
