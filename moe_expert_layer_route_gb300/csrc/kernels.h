@@ -32,8 +32,10 @@ cudaError_t launch_router_route(const void *x, const void *w_r, const float *bia
 // dX += dlogits W_r (bf16 in/out) and dW_r = dlogits^T x (fp32), the latter through
 // router_dw_splits(T, d, E) token splits whose partials (E*d floats each) go to part
 int router_dw_splits(int T, int d, int E);
-cudaError_t launch_router_backward(const void *x, const void *w_r, const float *dlogits, void *dx,
-                                   float *dw, float *part, int T, int d, int E, cudaStream_t st);
+cudaError_t launch_router_dx(const void *w_r, const float *dlogits, void *dx, int T, int d,
+                             int E, cudaStream_t st);
+cudaError_t launch_router_dw(const void *x, const float *dlogits, float *dw, float *part, int T,
+                             int d, int E, cudaStream_t st);
 cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,
                             float *dlogits, int T, int E, int k, cudaStream_t st);
 cudaError_t launch_count(const int32_t *ids, int32_t *rank, int32_t *hist, int T, int E, int k,

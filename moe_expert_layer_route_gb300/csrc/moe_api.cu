@@ -3,6 +3,8 @@
 // grouped_gemm.cu; this file only validates, carves workspaces and orders launches.
 #include <atomic>
 #include <mutex>
+#include <set>
+#include <string>
 #include <vector>
 
 #include "../../include/moe_gb300.h"
@@ -102,6 +104,37 @@ moe_status check_ptrs(P... ptrs) {
   return MOE_OK;
 }
 
+// A second stream per device for independent kernels of one call that run side by
+// side (the router GEMM's two gradients). Each use is a fork (event on the caller's
+// stream, waited by the side stream) and a join (event on the side stream, waited by
+// the caller's stream) enqueued under one lock, so the calls of several host threads
+// do not interleave their event records.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+// The side stream of the current device, or null (then the work stays on the caller's
+// stream). Call with g_side_mu held.
+SideStream *side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  SideStream &sd = g_side[dev & 63];
+  if (!sd.tried) {
+    sd.tried = true;
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      sd.s = nullptr;
+      cudaGetLastError();
+    }
+  }
+  return sd.s ? &sd : nullptr;
+}
+
 moe_status check_device() {
   static int ok[64] = {};  // 0 unknown, 1 good, -1 unsupported
   int dev = 0;
@@ -140,6 +173,22 @@ struct Prof {
   bool pending = false;
 } g_prof;
 
+
+bool on_side_stream(cudaStream_t st) {
+  if (!st) return false;
+  for (const SideStream &sd : g_side)
+    if (sd.s == st) return true;
+  return false;
+}
+
+// "<name> (overlapped)", interned (the profile keeps the pointers)
+const char *overlapped_name(const char *name) {
+  static std::mutex mu;
+  static std::set<std::string> names;
+  std::lock_guard<std::mutex> lock(mu);
+  return names.insert(std::string(name) + " (overlapped)").first->c_str();
+}
+
 }  // namespace
 
 namespace moe {
@@ -156,7 +205,8 @@ cudaError_t note_launch(const char *name, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_prof.on && g_prof.pending) {
     cudaEventRecord(g_prof.stop[g_prof.used], st);
-    g_prof.names[g_prof.used] = name;
+    // a launch on the side stream overlaps others: its events span them too
+    g_prof.names[g_prof.used] = on_side_stream(st) ? overlapped_name(name) : name;
     ++g_prof.used;
     g_prof.pending = false;
   }
@@ -430,9 +480,22 @@ moe_status moe_router_backward(moe_shape s, const moe_bf16 *x, const moe_bf16 *w
     MOE_CUDA(cudaMemsetAsync(dw_router, 0, (size_t)s.E * s.d * sizeof(float), st));
     return MOE_OK;
   }
-  MOE_CUDA(launch_router_backward(x, w_router, dlogits, dx, dw_router,
-                                  static_cast<float *>(scratch), (int)s.T, (int)s.d, (int)s.E,
-                                  st));
+  // dW_r (token splits, then their sum) runs beside the dX term on the side stream
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream *sd = side_stream();
+  cudaStream_t wst = st;
+  if (sd) {
+    MOE_CUDA(cudaEventRecord(sd->fork, st));
+    MOE_CUDA(cudaStreamWaitEvent(sd->s, sd->fork, 0));
+    wst = sd->s;
+  }
+  const cudaError_t ew = launch_router_dw(x, dlogits, dw_router, static_cast<float *>(scratch),
+                                          (int)s.T, (int)s.d, (int)s.E, wst);
+  if (sd) MOE_CUDA(cudaEventRecord(sd->join, sd->s));
+  const cudaError_t ex = launch_router_dx(w_router, dlogits, dx, (int)s.T, (int)s.d, (int)s.E, st);
+  if (sd) MOE_CUDA(cudaStreamWaitEvent(st, sd->join, 0));
+  MOE_CUDA(ew);
+  MOE_CUDA(ex);
   return MOE_OK;
 }
 

@@ -607,16 +607,18 @@ int router_dw_splits(int T, int d, int E) {
   return max(1, min(splits, chunks));
 }
 
-cudaError_t launch_router_backward(const void *x, const void *w_r, const float *dlogits, void *dx,
-                                   float *dw, float *part, int T, int d, int E, cudaStream_t st) {
+cudaError_t launch_router_dx(const void *w_r, const float *dlogits, void *dx, int T, int d,
+                             int E, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
   const dim3 bdx((T + kRbRows - 1) / kRbRows, (d + kRbCols - 1) / kRbCols);
-  if (T > 0) {
-    launch_begin(st);
-    router_dx_kernel<<<bdx, 256, 0, st>>>(dlogits, static_cast<const uint4 *>(w_r),
-                                          static_cast<uint4 *>(dx), T, d, E);
-    cudaError_t e = note_launch("router_dx", st);
-    if (e != cudaSuccess) return e;
-  }
+  launch_begin(st);
+  router_dx_kernel<<<bdx, 256, 0, st>>>(dlogits, static_cast<const uint4 *>(w_r),
+                                        static_cast<uint4 *>(dx), T, d, E);
+  return note_launch("router_dx", st);
+}
+
+cudaError_t launch_router_dw(const void *x, const float *dlogits, float *dw, float *part, int T,
+                             int d, int E, cudaStream_t st) {
   const int splits = router_dw_splits(T, d, E);
   const int chunks = max(1, (T + 31) / 32);
   const int split_tokens = ((chunks + splits - 1) / splits) * 32;
