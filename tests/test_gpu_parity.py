@@ -161,6 +161,7 @@ BWD_CASES = [
     (1, 64, 4, 2, 64, 45, False),
     (1024, 256, 4, 2, 320, 46, False),   # SM-pair GEMMs (see FFN_CASES)
     (900, 200, 3, 2, 200, 47, False),
+    (1024, 384, 4, 2, 576, 48, False),   # pairs with 192-wide dgrad tiles (d, f multiples of 192)
 ]
 
 
