@@ -109,6 +109,21 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 OVERLAPPED = " (overlapped)"
 
 
+def gemm_bytes(wl: workloads.Workload, training: bool) -> dict:
+    """Algorithmic HBM bytes of each grouped GEMM launch: its weights, and its activation
+    rows read and written once (A = T*k rows; segment padding not counted)."""
+    A, d, f, E = wl.A, wl.d, wl.f, wl.E
+    wgu, wdown = E * d * 2 * f * 2, E * f * d * 2
+    return {
+        "gemm_gate_up_swiglu": wgu + A * d * 2 + A * f * 2 + (A * 2 * f * 2 if training else 0),
+        "gemm_down": wdown + A * f * 2 + A * d * 2,
+        "gemm_dgrad_h_swiglu_bwd": wdown + A * d * 2 + 2 * A * 2 * f * 2,
+        "gemm_wgrad_down": A * f * 2 + A * d * 2 + wdown,
+        "gemm_dgrad_x": wgu + A * 2 * f * 2 + A * d * 2,
+        "gemm_wgrad_gu": A * d * 2 + A * 2 * f * 2 + wgu,
+    }
+
+
 def router_splits(T: int, d: int, E: int) -> int:
     cells = -(-d // 256) * -(-E // 32)
     return max(1, min(-(-304 // cells), -(-T // 32)))
@@ -399,6 +414,22 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     gemm_flop = sum(work[n][1] * len(per[n]) for n in gemm_names) / K
     gemm_ms = sum(sum(per[n]) for n in gemm_names) / K
     gemm_tflops = gemm_flop / (gemm_ms * 1e-3) / 1e12
+    # the whole step against its roofline: the slower of its FLOPs at the bf16 peak and
+    # its algorithmic bytes (every stage's, GEMMs included) at the HBM copy rate
+    gb = gemm_bytes(wl, wl.backward)
+    step_bytes = 0.0
+    for n, ts in serial.items():
+        kind, amount = work.get(n, ("byte", 0))
+        step_bytes += (gb[n] if n in gb else amount if kind == "byte" else 0) * len(ts)
+    step_bytes /= K
+    t_flop = gemm_flop / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    t_bytes = step_bytes / (pk["hbm_gbs"] * 1e9) * 1e3
+    step_roofline = {"flop": gemm_flop, "bytes": step_bytes, "t_flop_ms": t_flop,
+                     "t_bytes_ms": t_bytes, "bound": "tensor" if t_flop >= t_bytes else "hbm",
+                     "frac": max(t_flop, t_bytes) / ms}
+    counts = views["counts"].cpu().numpy()
+    experts = {"max": int(counts.max()), "min": int(counts.min()),
+               "empty": int((counts == 0).sum())}
 
     # ---- end to end through the Python API with host buffers
     e2e = None
@@ -462,6 +493,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "gemm_tflops": gemm_tflops,
         "gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16_tflops_sustained"],
         "gemm_flop_per_step": gemm_flop,
+        "ms_per_step_median": statistics.median(step_ms),
+        "step_roofline": step_roofline,
+        "experts": experts,
         "roofline": roof,
         "stages": stages,
         "gpu_launches": launches,
