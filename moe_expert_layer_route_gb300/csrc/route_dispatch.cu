@@ -260,16 +260,19 @@ __global__ void __launch_bounds__(256) scatter_kernel(
 }
 
 // ------------------------------------------------------------------------- combine
-// One warp per token: y[t] = sum_j w[t][j] * o[row_of[t][j]], fp32 FMA in slot order,
-// one bf16 rounding. With unit weights it is the backward's dX gather-sum.
-template <bool WEIGHTED>
+// WPT warps per token, each on every WPT-th 32-vector slice of the row:
+// y[t] = sum_j w[t][j] * o[row_of[t][j]], fp32 FMA in slot order, one bf16 rounding.
+// With unit weights it is the backward's dX gather-sum. Several warps per row shorten
+// each warp's chain of dependent row loads (the kernel is latency-bound below ~1 GB).
+template <bool WEIGHTED, int WPT>
 __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict__ o,
                                                          const float *__restrict__ w,
                                                          const int32_t *__restrict__ row_of,
                                                          uint4 *__restrict__ y, int T, int nvec,
                                                          int k) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const int t = blockIdx.x * (8 / WPT) + warp / WPT;
+  const int seg = warp % WPT;
   if (t >= T) return;
   int row = 0;
   float wt = 1.f;
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict
     rows[j] = __shfl_sync(0xffffffffu, row, j);
     wts[j] = __shfl_sync(0xffffffffu, wt, j);
   }
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = seg * 32 + lane; v < nvec; v += 32 * WPT) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -536,12 +539,26 @@ cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *ran
   return note_launch("scatter", st);
 }
 
+// warps per token of the gather kernels: more for longer rows (at least 64 vectors each)
+template <bool WEIGHTED>
+static void launch_gather(const void *o, const float *w, const int32_t *row_of, void *y, int T,
+                          int nvec, int k, cudaStream_t st) {
+  if (nvec >= 256)
+    gather_sum_kernel<WEIGHTED, 4><<<ceil_div(T, 2), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+  else if (nvec >= 128)
+    gather_sum_kernel<WEIGHTED, 2><<<ceil_div(T, 4), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+  else
+    gather_sum_kernel<WEIGHTED, 1><<<ceil_div(T, 8), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+}
+
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of, void *y, int T,
                            int d, int k, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   launch_begin(st);
-  gather_sum_kernel<true><<<ceil_div(T, 8), 256, 0, st>>>((const uint4 *)o, w, row_of,
-                                                          (uint4 *)y, T, d / 8, k);
+  launch_gather<true>(o, w, row_of, y, T, d / 8, k, st);
   return note_launch("combine", st);
 }
 
@@ -549,8 +566,7 @@ cudaError_t launch_gather_sum(const void *dxp, const int32_t *row_of, void *dx, 
                               int k, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   launch_begin(st);
-  gather_sum_kernel<false><<<ceil_div(T, 8), 256, 0, st>>>((const uint4 *)dxp, nullptr, row_of,
-                                                           (uint4 *)dx, T, d / 8, k);
+  launch_gather<false>(dxp, nullptr, row_of, dx, T, d / 8, k, st);
   return note_launch("dx_gather", st);
 }
 
