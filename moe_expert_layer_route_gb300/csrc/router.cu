@@ -14,7 +14,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kKB = 64;          // k per staged block: one 128-byte TMA row of bf16
+constexpr int kSub = 2;          // 64-column TMA boxes (one 128-byte row each) per stage
+constexpr int kKB = 64 * kSub;   // k per staged block
 
 // acc = a * b + acc for the bf16 in the low (HI = false) or high half of a and b: the
 // exact product of two bf16 values added to the fp32 accumulator with one rounding
@@ -205,9 +206,9 @@ __host__ __device__ constexpr size_t route_lanes_work() {
 // them), then expert group eg; the thread owns tokens tg + (32/TT) j and experts
 // eg + EG j. EP = EG * TE >= E.
 //
-// Staging, per block of 64 k: one thread issues two TMA loads (x rows [32c, 32c+32),
-// W_r rows [0, EP), 128-byte swizzle: 16-byte chunk j of row r lands at chunk
-// j ^ (r % 8)) into a ring of S stages; rows past T or E and columns past d arrive as
+// Staging, per block of 128 k: one thread issues TMA loads of two 64-column boxes each
+// of the x rows [32c, 32c+32) and of the W_r rows [0, EP) (128-byte swizzle: 16-byte
+// chunk j of row r lands at chunk j ^ (r % 8)) into a ring of S stages; rows past T or E and columns past d arrive as
 // zeros. The arithmetic reads its bf16 operands straight from the stage, 8 k per
 // 16-byte load (the swizzle spreads the few rows a warp reads over distinct banks), and
 // runs the chains with the mixed-precision fma. A barrier per block frees the stage
@@ -223,7 +224,8 @@ __global__ void __launch_bounds__((32 / TT) * EG, 1) router_route_kernel(
   constexpr int NT = TG * EG;
   constexpr int EP = EG * TE;
   constexpr int ROWS = kChunk + EP;
-  constexpr int STAGE = ROWS * 128;         // bytes of one ring stage
+  constexpr int SUB = ROWS * 128;           // bytes of one 64-column sub-block
+  constexpr int STAGE = SUB * kSub;         // bytes of one ring stage
   static_assert(kChunk % TT == 0 && NT % 32 == 0 && EP % 8 == 0, "tile");
   static_assert((size_t)S * STAGE >= 2 * sizeof(float) * kChunk * (EP + 1) +
                     route_lanes_work<NT / 32>(), "epilogue space");
@@ -247,8 +249,11 @@ __global__ void __launch_bounds__((32 / TT) * EG, 1) router_route_kernel(
   auto issue = [&](int b) {  // thread 0: block b into stage b % S
     uint8_t *dst = smem + (b % S) * STAGE;
     mbar_arrive_expect_tx(&full[b % S], STAGE);
-    tma_load_2d(dst, &tm_x, &full[b % S], b * kKB, t0);
-    tma_load_2d(dst + kChunk * 128, &tm_w, &full[b % S], b * kKB, 0);
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) {
+      tma_load_2d(dst + u * SUB, &tm_x, &full[b % S], b * kKB + 64 * u, t0);
+      tma_load_2d(dst + u * SUB + kChunk * 128, &tm_w, &full[b % S], b * kKB + 64 * u, 0);
+    }
   };
   if (tid == 0)
     for (int b = 0; b < S && b < nblk; ++b) issue(b);
@@ -295,30 +300,34 @@ __global__ void __launch_bounds__((32 / TT) * EG, 1) router_route_kernel(
   bool fail = __syncthreads_or(!mbar_wait(&full[0], 0, status)) != 0;
   int b = 0;
   for (; b < nblk && !fail; ++b) {
-    const uint8_t *sb = smem + (b % S) * STAGE;
-    uint4 xA[TT], wA[TE], xB[TT], wB[TE];  // two register sets: the next chunk loads early
+    const uint8_t *sbase = smem + (b % S) * STAGE;
+#pragma unroll 1
+    for (int u = 0; u < kSub; ++u) {  // the stage's 64-column sub-blocks in k order
+      const uint8_t *sb = sbase + u * SUB;
+      uint4 xA[TT], wA[TE], xB[TT], wB[TE];  // two register sets: the next chunk loads early
 #pragma unroll
-    for (int a = 0; a < TT; ++a) xA[a] = *reinterpret_cast<const uint4 *>(sb + xo[a]);
+      for (int a = 0; a < TT; ++a) xA[a] = *reinterpret_cast<const uint4 *>(sb + xo[a]);
 #pragma unroll
-    for (int e = 0; e < TE; ++e) wA[e] = *reinterpret_cast<const uint4 *>(sb + wo[e]);
+      for (int e = 0; e < TE; ++e) wA[e] = *reinterpret_cast<const uint4 *>(sb + wo[e]);
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-#pragma unroll
-      for (int a = 0; a < TT; ++a)
-        xB[a] = *reinterpret_cast<const uint4 *>(sb + (xo[a] ^ ((j + 1) << 4)));
-#pragma unroll
-      for (int e = 0; e < TE; ++e)
-        wB[e] = *reinterpret_cast<const uint4 *>(sb + (wo[e] ^ ((j + 1) << 4)));
-      fma_chunk(xA, wA);
-      if (j + 2 < 8) {
+      for (int j = 0; j < 8; j += 2) {
 #pragma unroll
         for (int a = 0; a < TT; ++a)
-          xA[a] = *reinterpret_cast<const uint4 *>(sb + (xo[a] ^ ((j + 2) << 4)));
+          xB[a] = *reinterpret_cast<const uint4 *>(sb + (xo[a] ^ ((j + 1) << 4)));
 #pragma unroll
         for (int e = 0; e < TE; ++e)
-          wA[e] = *reinterpret_cast<const uint4 *>(sb + (wo[e] ^ ((j + 2) << 4)));
+          wB[e] = *reinterpret_cast<const uint4 *>(sb + (wo[e] ^ ((j + 1) << 4)));
+        fma_chunk(xA, wA);
+        if (j + 2 < 8) {
+#pragma unroll
+          for (int a = 0; a < TT; ++a)
+            xA[a] = *reinterpret_cast<const uint4 *>(sb + (xo[a] ^ ((j + 2) << 4)));
+#pragma unroll
+          for (int e = 0; e < TE; ++e)
+            wA[e] = *reinterpret_cast<const uint4 *>(sb + (wo[e] ^ ((j + 2) << 4)));
+        }
+        fma_chunk(xB, wB);
       }
-      fma_chunk(xB, wB);
     }
     const bool ok = b + 1 >= nblk || mbar_wait(&full[(b + 1) % S], ((b + 1) / S) & 1, status);
     fail = __syncthreads_or(!ok) != 0;
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__((32 / TT) * EG, 1) router_route_kernel(
 
 template <int TT, int TE, int EG, int S>
 constexpr size_t router_smem() {
-  return (size_t)S * (kChunk + EG * TE) * 128 + 1024;  // + alignment slack
+  return (size_t)S * (kChunk + EG * TE) * 128 * kSub + 1024;  // + alignment slack
 }
 
 template <int TT, int TE, int EG, int S, bool COUNT>
@@ -412,7 +421,7 @@ cudaError_t launch_router_as(const void *x, const void *w_r, const float *bias, 
   CUtensorMap tm_x, tm_w;
   const uint64_t sx[1] = {(uint64_t)d * 2};
   const uint64_t dx[2] = {(uint64_t)d, (uint64_t)T}, dw[2] = {(uint64_t)d, (uint64_t)E};
-  const uint32_t bx[2] = {(uint32_t)kKB, (uint32_t)kChunk}, bw[2] = {(uint32_t)kKB, (uint32_t)EP};
+  const uint32_t bx[2] = {64u, (uint32_t)kChunk}, bw[2] = {64u, (uint32_t)EP};
   cudaError_t e = encode_tensor_map(&tm_x, x, 2, dx, sx, bx, 128);
   if (e == cudaSuccess) e = encode_tensor_map(&tm_w, w_r, 2, dw, sx, bw, 128);
   if (e != cudaSuccess) return e;
@@ -430,12 +439,12 @@ cudaError_t launch_router_cfg(const void *x, const void *w_r, const float *bias,
 #define MOE_ROUTER(TT, TE, EG, S)                                                             \
   return launch_router_as<TT, TE, EG, S, COUNT>(x, w_r, bias, logits, ids, w, rank, hist,    \
                                                 prob_part, status, T, d, E, k, C, st)
-  if (E <= 8) MOE_ROUTER(4, 1, 8, 12);
-  if (E <= 16) MOE_ROUTER(4, 2, 8, 12);
-  if (E <= 32) MOE_ROUTER(4, 2, 16, 6);
-  if (E <= 64) MOE_ROUTER(4, 4, 16, 6);
-  if (E <= 128) MOE_ROUTER(4, 4, 32, 5);
-  MOE_ROUTER(8, 4, 64, 4);
+  if (E <= 8) MOE_ROUTER(4, 1, 8, 6);
+  if (E <= 16) MOE_ROUTER(4, 2, 8, 6);
+  if (E <= 32) MOE_ROUTER(4, 2, 16, 3);
+  if (E <= 64) MOE_ROUTER(4, 4, 16, 3);
+  if (E <= 128) MOE_ROUTER(4, 4, 32, 3);
+  MOE_ROUTER(8, 4, 64, 2);
 #undef MOE_ROUTER
 }
 
