@@ -517,42 +517,67 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float *__restrict_
 
 // dW partials: block (column block, expert block, token split). Token tiles of 32;
 // each split sums its tokens in order into part[split][e][i] (or straight into dW when
-// there is one split).
+// there is one split). The next tile's loads wait in registers while the current tile
+// is summed (two shared-memory buffers, one barrier per tile).
 __global__ void __launch_bounds__(256) router_dw_kernel(const float *__restrict__ dl,
                                                         const uint4 *__restrict__ x,
                                                         float *__restrict__ part, int T, int d,
                                                         int E, int split_tokens) {
   constexpr int TB = 32;
-  __shared__ __align__(16) float s_dl[TB][kRbRows];        // [token][expert]
-  __shared__ __align__(16) uint4 s_x[TB][kRbCols / 8];     // [token][8-column vector]
+  constexpr int XV = TB * (kRbCols / 8) / 256;             // x vectors per thread per tile
+  __shared__ __align__(16) float s_dl[2][TB][kRbRows];     // [buf][token][expert]
+  __shared__ __align__(16) uint4 s_x[2][TB][kRbCols / 8];  // [buf][token][8-column vector]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c0 = blockIdx.x * kRbCols, e0 = blockIdx.y * kRbRows;
   const int ts = blockIdx.z;
   const int tbeg = ts * split_tokens, tend = min(T, tbeg + split_tokens);
   const int nvr = d >> 3, v = (c0 >> 3) + lane;
+  // this thread's staging work: dl value (token dt, expert de), x vectors (token xt[i],
+  // column vector xc)
+  const int dt = threadIdx.x / kRbRows, de = threadIdx.x % kRbRows;  // 8 tokens x 32 experts
+  const int xc = threadIdx.x % (kRbCols / 8), xt0 = threadIdx.x / (kRbCols / 8);
+  float rdl[TB * kRbRows / 256];
+  uint4 rx[XV];
+  auto fetch = [&](int t0) {
+    const int nt = min(TB, tend - t0);
+#pragma unroll
+    for (int i = 0; i < TB * kRbRows / 256; ++i) {
+      const int t = dt + 8 * i;
+      rdl[i] = (t < nt && e0 + de < E) ? dl[(int64_t)(t0 + t) * E + e0 + de] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < XV; ++i) {
+      const int t = xt0 + (256 / (kRbCols / 8)) * i;
+      const int vv = (c0 >> 3) + xc;
+      rx[i] = (t < nt && vv < nvr) ? ldg_nc(x + (int64_t)(t0 + t) * nvr + vv)
+                                   : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < TB * kRbRows / 256; ++i) s_dl[buf][dt + 8 * i][de] = rdl[i];
+#pragma unroll
+    for (int i = 0; i < XV; ++i) s_x[buf][xt0 + (256 / (kRbCols / 8)) * i][xc] = rx[i];
+  };
   float acc[4][8];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
-  for (int t0 = tbeg; t0 < tend; t0 += TB) {
+  if (tbeg < tend) {
+    fetch(tbeg);
+    stash(0);
+  }
+  __syncthreads();
+  int buf = 0;
+  for (int t0 = tbeg; t0 < tend; t0 += TB, buf ^= 1) {
     const int nt = min(TB, tend - t0);
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < TB * kRbRows; idx += 256) {
-      const int t = idx / kRbRows, e = idx % kRbRows;
-      s_dl[t][e] = (t < nt && e0 + e < E) ? dl[(int64_t)(t0 + t) * E + e0 + e] : 0.f;
-    }
-    for (int idx = threadIdx.x; idx < TB * (kRbCols / 8); idx += 256) {
-      const int t = idx / (kRbCols / 8), c = idx % (kRbCols / 8);
-      const int vv = (c0 >> 3) + c;
-      s_x[t][c] = (t < nt && vv < nvr) ? ldg_nc(x + (int64_t)(t0 + t) * nvr + vv)
-                                       : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
+    const bool more = t0 + TB < tend;
+    if (more) fetch(t0 + TB);
     for (int t = 0; t < nt; ++t) {
-      const float4 g = *reinterpret_cast<const float4 *>(&s_dl[t][4 * warp]);
+      const float4 g = *reinterpret_cast<const float4 *>(&s_dl[buf][t][4 * warp]);
       float xv[8];
-      unpack8(s_x[t][lane], xv);
+      unpack8(s_x[buf][t][lane], xv);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         acc[0][j] = fmaf(g.x, xv[j], acc[0][j]);
@@ -561,6 +586,8 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const float *__restrict_
         acc[3][j] = fmaf(g.w, xv[j], acc[3][j]);
       }
     }
+    if (more) stash(buf ^ 1);  // the other buffer was last read before the previous barrier
+    __syncthreads();
   }
   if (v >= nvr) return;
   float *out = part + (int64_t)ts * E * d;
