@@ -330,14 +330,14 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     moe.check_device_status(ws)
     moe.check_device_status(scratch)
 
-    # ---- device-timed region
+    # ---- device-timed region (no instrumentation inside: the library's per-launch
+    # events of the profiled pass below would add their own gaps to the step)
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
     launches0 = moe.launch_count()
-    moe.profile_start(capacity=K * 24)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clk:
@@ -348,13 +348,23 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
             ends[i].record()
         torch.cuda.synchronize()
     barrier(world)
-    records = moe.profile_stop(capacity=K * 24)
     launches = moe.launch_count() - launches0
     moe.check_device_status(ws)
     moe.check_device_status(scratch)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     tokens_all = sum_over_ranks(wl.T, world, dev)
+
+    # ---- profiled pass: the same K steps with an event pair around every launch, for
+    # the per-kernel times, shares and the dominant kernel's roofline
+    moe.profile_start(capacity=K * 24)
+    for i in range(K):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    records = moe.profile_stop(capacity=K * 24)
+    moe.check_device_status(ws)
+    moe.check_device_status(scratch)
 
     # ---- per-kernel times and the roofline of the dominant kernel
     per = {}
@@ -431,6 +441,31 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     experts = {"max": int(counts.max()), "min": int(counts.min()),
                "empty": int((counts == 0).sum())}
 
+    # ---- the same step captured once in a CUDA graph and replayed (the calls allocate
+    # nothing and never synchronise, so they capture): device time without launch gaps
+    graph = None
+    if not args.no_graph:
+        gstream = torch.cuda.Stream(device=dev)
+        gstream.wait_stream(torch.cuda.current_stream(dev))
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gstream):
+            step()
+        cg.replay()
+        torch.cuda.synchronize()
+        gs = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ge = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        barrier(world)
+        for i in range(K):
+            flush.zero_()
+            gs[i].record()
+            cg.replay()
+            ge[i].record()
+        torch.cuda.synchronize()
+        gms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(gs, ge)), world,
+                             dev)
+        graph = {"ms_per_step": gms, "value": tokens_all / (gms * 1e-3), "unit": UNIT}
+        del cg
+
     # ---- end to end through the Python API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -496,6 +531,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         "ms_per_step_median": statistics.median(step_ms),
         "step_roofline": step_roofline,
         "experts": experts,
+        "graph": graph,
         "roofline": roof,
         "stages": stages,
         "gpu_launches": launches,
@@ -557,6 +593,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing of the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--router-grad", action="store_true",
