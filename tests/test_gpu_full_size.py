@@ -10,7 +10,7 @@ import torch
 import oracle
 import workloads
 from gpu_cases import check_dispatch_exact, to_np
-from tolerance import W_REL, assert_close
+from tolerance import W_REL, assert_close, assert_close_selected
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -73,7 +73,10 @@ def test_workload_full_size(moe, name):
     assert_close(to_np(dx[torch.from_numpy(toks).to(dev)]), dx_ref, "dX (sampled tokens)")
     dl_ref = np.stack([oracle.router_backward_token(x64[i], dy64[i], rid[t], rw[t], wl.E, WG, WD)
                        for i, t in enumerate(toks)])
-    assert_close(to_np(dl[torch.from_numpy(toks).to(dev)]), dl_ref, "dlogits (sampled tokens)")
+    chosen = np.zeros(dl_ref.shape, dtype=bool)
+    np.put_along_axis(chosen, rid[toks].astype(np.int64), True, axis=1)
+    assert_close_selected(to_np(dl[torch.from_numpy(toks).to(dev)]), dl_ref, chosen,
+                          "dlogits (sampled tokens)")
 
     counts = ref["counts"]
     experts = {int(np.argmax(counts)), int(np.argmin(counts)), int(rng.integers(wl.E))}

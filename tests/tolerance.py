@@ -11,7 +11,12 @@ wrong term or index does. The expert weight gradients dW_gu and dW_down are E
 independent matrices whose scales follow each expert's load (a skewed load gives
 one expert every token and leaves others empty), so they are checked expert by
 expert (assert_close_experts): each non-empty expert's slice against the bound,
-each empty expert's slice exactly zero.
+each empty expert's slice exactly zero. The router-logit gradient is sparse: a token's
+row is nonzero only at its k chosen experts, so it is checked on those entries
+(assert_close_selected: the bounds with the norm and rms taken over the chosen entries)
+and must be exactly zero elsewhere; over all T x E entries the (E - k) / E exact zeros
+would shrink the rms floor until the bf16 rounding of the expert outputs it is formed
+from exceeds the element bound.
 
 Setting MOE_PARITY_LOG=<file> appends every checked error to that file.
 """
@@ -72,3 +77,16 @@ def assert_close_experts(got, ref, name: str = "") -> None:
         with open(log, "a") as fh:
             fh.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]}\t{name} "
                      f"(worst expert)\tnormwise={worst[0]:.3e}\telementwise={worst[1]:.3e}\n")
+
+
+def assert_close_selected(got, ref, selected, name: str = "") -> tuple[float, float]:
+    """Check a gradient that is nonzero only where `selected` (see the module docstring):
+    exactly zero elsewhere, the bounds over the selected entries."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    selected = np.asarray(selected, dtype=bool)
+    assert got.shape == ref.shape == selected.shape
+    assert not got[~selected].any(), f"{name}: entries outside the selection must be zero"
+    assert not ref[~selected].any(), f"{name}: the reference is nonzero outside the selection"
+    return assert_close(got[selected], ref[selected], name + " (chosen experts)")
+
