@@ -31,14 +31,21 @@ namespace {
 // CTA a k-block then moves 32 KB instead of 48 KB, which leaves room for 6 stages.
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
+// A pipeline stage holds kSub K-blocks of 64 (each its own 128-byte-swizzled A and B
+// tiles): the MMA issuer waits for, and commits, one stage of kSub * 4 MMAs at a time.
+// Measured on GB300: a barrier round costs about as much as two or three MMAs, so
+// stages of 128 K run faster than stages of 64 K with the same bytes in flight.
+constexpr int kSub = 2;
+constexpr int BKS = BK * kSub;  // K per stage
 
 template <bool PAIR>
 struct Cfg {
   static constexpr int kMTile = PAIR ? 2 * BM : BM;  // rows of one (pair-)tile
   static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows (N) each CTA loads
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStages = (PAIR ? 6 : 4) / kSub;
   static constexpr int kBBytes = kBRows * BK * 2;    // 16 or 32 KB
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSubBytes = kABytes + kBBytes;  // one K-block of 64
+  static constexpr int kStageBytes = kSub * kSubBytes;
 };
 constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box (MN-major tiles are built of these)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of the columns
@@ -72,7 +79,8 @@ struct Args {
   int E;
   int n_tiles;  // tiles along N
   int m_tiles;  // WGRAD: (pair-)tiles along M of one expert's dW
-  int k_tiles;  // ragged-M kinds: K / 64, rounded up
+  int k_tiles;  // ragged-M kinds: K / BKS, rounded up
+  int k_last;   // ragged-M kinds: 16-wide K slices of the last stage that hold columns
   int weight_stationary;  // ragged-M tile order
   int M_out;    // WGRAD: rows of dW[e]
   int N_out;    // valid output columns
@@ -91,7 +99,7 @@ struct Args {
 // feed the MMA but nothing is stored).
 struct Tile {
   int e, m0, n0, kt, kr0;
-  int klast;  // 16-row K slices of the last k-block that hold rows (WGRAD; else 4)
+  int klast;  // 16-wide K slices of the last stage that hold data (at most 4 * kSub)
   bool valid;
 };
 
@@ -107,7 +115,7 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
   constexpr int kMTile = Cfg<PAIR>::kMTile;
   Tile t;
   t.valid = true;
-  t.klast = BK / 16;
+  t.klast = BKS / 16;
   if (KIND == WGRAD) {
     const int per = a.m_tiles * a.n_tiles;
     t.e = tile / per;
@@ -115,10 +123,10 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
     t.m0 = (r / a.n_tiles) * kMTile + rank * BM;
     t.n0 = (r % a.n_tiles) * BN;
     t.kr0 = a.padded[t.e];
-    t.kt = (a.counts[t.e] + BK - 1) / BK;  // k-blocks holding the expert's rows
-    // the last k-block's rows past the count are zero padding: its MMAs stop at the
-    // last 16-row slice that holds a row
-    t.klast = (a.counts[t.e] - (t.kt - 1) * BK + 15) / 16;
+    t.kt = (a.counts[t.e] + BKS - 1) / BKS;  // stages holding the expert's rows
+    // the last stage's rows past the count are zero padding or other experts' rows:
+    // its MMAs stop at the last 16-row slice that holds a row of this expert
+    t.klast = (a.counts[t.e] - (t.kt - 1) * BKS + 15) / 16;
     return t;
   }
   // ragged M: "units" are 128-row tiles (single) or pairs of them (pair mode);
@@ -148,6 +156,7 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
   t.m0 = mt * BM;
   t.n0 = nt * (KIND == GATE_UP ? BN / 2 : BN);
   t.kt = a.k_tiles;
+  t.klast = a.k_last;
   t.kr0 = 0;
   return t;
 }
@@ -487,9 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *sA = smem + s * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], (kPair ? 2 : 1) * kStageBytes);
           const uint32_t bar_pair = kPair ? mapa_shared(&full_bar[s], 0) : 0;
-          if (issued != a.withhold_kblock)
-            issue_loads<KIND, PAIR>(&tmA, &tmB, sA, sA + kABytes, &full_bar[s], bar_pair, t, kb,
-                                    rank);
+          if (issued != a.withhold_kblock) {
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+              uint8_t *sj = sA + j * Cfg<PAIR>::kSubBytes;
+              issue_loads<KIND, PAIR>(&tmA, &tmB, sj, sj + kABytes, &full_bar[s], bar_pair, t,
+                                      kb * kSub + j, rank);
+            }
+          }
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -543,16 +557,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_base + s * kStageBytes;
-            const uint32_t b_addr = a_addr + kABytes;
-            const int nk = (kb == t.kt - 1) ? t.klast : BK / 16;
+            const int nk = (kb == t.kt - 1) ? t.klast : BKS / 16;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              if (kk < nk) {
-                const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
-                const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
-                if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
-                else tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+            for (int j = 0; j < kSub; ++j) {
+              const uint32_t a_addr = smem_base + s * kStageBytes + j * Cfg<PAIR>::kSubBytes;
+              const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                if (j * (BK / 16) + kk < nk) {
+                  const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
+                  const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
+                  const uint32_t acc = (kb | j | kk) != 0;
+                  if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, acc);
+                  else tc_mma_bf16(d_tmem, ad, bd, kIdesc, acc);
+                }
               }
             }
             any = true;
@@ -722,6 +740,13 @@ cudaError_t launch_kind(bool pair, const CUtensorMap &tmA, const CUtensorMap &tm
               : launch_kind_as<KIND, false>(tmA, tmB, tmO, tmO2, a, max_tiles, name, st);
 }
 
+// K extent of a ragged-M GEMM: its stages of BKS and the 16-wide slices of the last one
+// that hold columns (the MMAs past them would only add the TMA's zero fill).
+void set_k(Args &a, int64_t K) {
+  a.k_tiles = cdiv(K, BKS);
+  a.k_last = cdiv(K - (int64_t)(a.k_tiles - 1) * BKS, 16);
+}
+
 Args base_args(const GemmPlan &p, int *status) {
   Args a{};
   a.padded = p.padded;
@@ -798,7 +823,7 @@ cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, vo
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN / 2);
-  a.k_tiles = cdiv(d, BK);
+  set_k(a, d);
   a.N_out = f;
   a.f = f;
   a.out2 = gu;
@@ -818,7 +843,7 @@ cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
-  a.k_tiles = cdiv(f, BK);
+  set_k(a, f);
   a.N_out = d;
   const bool pair = pair_for_rows(p);
   return launch_kind<DOWN>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles, "gemm_down",
@@ -838,7 +863,7 @@ cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, c
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN);
-  a.k_tiles = cdiv(d, BK);
+  set_k(a, d);
   a.N_out = f;
   a.f = f;
   a.aux = gu;
@@ -860,7 +885,7 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
-  a.k_tiles = cdiv(2 * (int64_t)f, BK);
+  set_k(a, 2 * (int64_t)f);
   a.N_out = d;
   return launch_kind<DGRAD_X>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles,
                               "gemm_dgrad_x", st);

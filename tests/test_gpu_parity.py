@@ -53,6 +53,7 @@ FFN_CASES = [
     (1024, 256, 4, 2, 320, 17, False),
     (900, 200, 3, 2, 200, 18, False),
     (300, 64, 256, 16, 64, 19, False),   # the largest E and k: 256 experts of ~19 rows
+    (200, 64, 4, 2, 24, 20, False),      # f = 24: gate and up N tiles of 24 columns
 ]
 
 
@@ -135,7 +136,8 @@ def test_expert_ffn_parity(moe, c):
     pad = np.ones(int(to_np(disp["padded_offsets"])[-1]), dtype=bool)
     pad[grow] = False
     if pad.any():
-        assert not to_np(o)[:len(pad)][pad].any() and not to_np(h)[:len(pad)][pad].any()
+        for t in (o, h, gu):
+            assert not to_np(t)[:len(pad)][pad].any()
 
 
 @pytest.mark.parametrize("c", FFN_CASES, ids=_ids)
@@ -164,6 +166,7 @@ BWD_CASES = [
     (900, 200, 3, 2, 200, 47, False),
     (1024, 384, 4, 2, 576, 48, False),   # pairs with N tails in every GEMM (384, 576, 1152)
     (300, 64, 256, 16, 64, 49, False),   # the largest E and k
+    (333, 72, 3, 2, 40, 50, False),      # K tail of 8 (d = 72) and N tails of 40 (f = 40)
 ]
 
 
