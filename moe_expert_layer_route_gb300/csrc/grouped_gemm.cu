@@ -4,17 +4,21 @@
 // integration": grouped GEMM with a fused SwiGLU; "One trainer architecture": fused
 // experts as 3-D weight tensors) run as one persistent kernel per GEMM over all
 // experts. Design:
-//   * one CTA per SM, 192 threads: warp 0 issues TMA loads, warp 1 issues
-//     tcgen05.mma (one elected lane), warps 2..5 run the epilogue out of TMEM;
-//   * tiles of 128 x 256 (M x N) with K steps of 64, 128-byte swizzled smem
-//     operands fed by cp.async.bulk.tensor into a 4-stage mbarrier ring;
+//   * one CTA per SM, 320 threads: warp 0 issues TMA loads, warp 1 issues tcgen05.mma
+//     (one elected lane), warps 2..9 run the epilogue out of TMEM (two per TMEM lane
+//     quarter, each on half of the tile's columns);
+//   * two forms: a CTA alone on a 128 x 256 (M x N) tile, or a 2-CTA cluster on a
+//     256 x 256 tile through the cta_group::2 MMA (each CTA loads its 128 A rows and
+//     half of B, the even CTA issues the MMAs);
+//   * 128-byte swizzled operands brought by cp.async.bulk.tensor into an mbarrier ring
+//     whose stages hold two K-blocks of 64 (192 KB in flight per CTA);
 //   * the fp32 accumulator lives in TMEM, two 256-column buffers so the epilogue of
 //     one tile overlaps the main loop of the next;
 //   * ragged per-expert M: expert segments are padded to 128 rows, so every M tile
 //     belongs to one expert and a device-side table maps tile -> expert (no host
 //     sync, the schedule reads the routing result from device memory);
-//   * ragged per-expert K (weight gradients): the K loop runs over the expert's
-//     padded rows, whose padding is zero in both operands.
+//   * ragged per-expert K (weight gradients): the K loop runs over the expert's rows
+//     and stops at the last 16-row slice that holds one.
 // Every output element is written by exactly one thread; nothing uses atomics.
 #include "kernels.h"
 
