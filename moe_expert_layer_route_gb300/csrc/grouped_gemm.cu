@@ -11,7 +11,8 @@
 //     256 x 256 tile through the cta_group::2 MMA (each CTA loads its 128 A rows and
 //     half of B, the even CTA issues the MMAs);
 //   * 128-byte swizzled operands brought by cp.async.bulk.tensor into an mbarrier ring
-//     whose stages hold two K-blocks of 64 (192 KB in flight per CTA);
+//     of 192 KB per CTA (pairs: 3 stages of two K-blocks of 64; single CTAs: 4 stages
+//     of one);
 //   * the fp32 accumulator lives in TMEM, two 256-column buffers so the epilogue of
 //     one tile overlaps the main loop of the next;
 //   * ragged per-expert M: expert segments are padded to 128 rows, so every M tile
@@ -35,17 +36,18 @@ namespace {
 // CTA a k-block then moves 32 KB instead of 48 KB, which leaves room for 6 stages.
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
-// A pipeline stage holds kSub K-blocks of 64 (each its own 128-byte-swizzled A and B
-// tiles): the MMA issuer waits for, and commits, one stage of kSub * 4 MMAs at a time.
-// Measured on GB300: a barrier round costs about as much as two or three MMAs, so
-// stages of 128 K run faster than stages of 64 K with the same bytes in flight.
-constexpr int kSub = 2;
-constexpr int BKS = BK * kSub;  // K per stage
 
 template <bool PAIR>
 struct Cfg {
   static constexpr int kMTile = PAIR ? 2 * BM : BM;  // rows of one (pair-)tile
   static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows (N) each CTA loads
+  // A pipeline stage holds kSub K-blocks of 64 (each its own 128-byte-swizzled A and
+  // B tiles): the MMA issuer waits for, and commits, one stage of kSub * 4 MMAs at a
+  // time. Measured on GB300: a barrier round costs about as much as two or three MMAs,
+  // so the pairs run faster on 3 stages of 128 K than on 6 of 64 K (same bytes in
+  // flight); the single-CTA form, whose K-blocks are 48 KB, keeps 4 stages of one.
+  static constexpr int kSub = PAIR ? 2 : 1;
+  static constexpr int kBKS = BK * kSub;  // K per stage
   static constexpr int kStages = (PAIR ? 6 : 4) / kSub;
   static constexpr int kBBytes = kBRows * BK * 2;    // 16 or 32 KB
   static constexpr int kSubBytes = kABytes + kBBytes;  // one K-block of 64
@@ -83,7 +85,7 @@ struct Args {
   int E;
   int n_tiles;  // tiles along N
   int m_tiles;  // WGRAD: (pair-)tiles along M of one expert's dW
-  int k_tiles;  // ragged-M kinds: K / BKS, rounded up
+  int k_tiles;  // ragged-M kinds: K / (K per stage), rounded up
   int k_last;   // ragged-M kinds: 16-wide K slices of the last stage that hold columns
   int weight_stationary;  // ragged-M tile order
   int M_out;    // WGRAD: rows of dW[e]
@@ -119,7 +121,7 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
   constexpr int kMTile = Cfg<PAIR>::kMTile;
   Tile t;
   t.valid = true;
-  t.klast = BKS / 16;
+  t.klast = Cfg<PAIR>::kBKS / 16;
   if (KIND == WGRAD) {
     const int per = a.m_tiles * a.n_tiles;
     t.e = tile / per;
@@ -127,10 +129,11 @@ __device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
     t.m0 = (r / a.n_tiles) * kMTile + rank * BM;
     t.n0 = (r % a.n_tiles) * BN;
     t.kr0 = a.padded[t.e];
-    t.kt = (a.counts[t.e] + BKS - 1) / BKS;  // stages holding the expert's rows
+    constexpr int kBKS = Cfg<PAIR>::kBKS;
+    t.kt = (a.counts[t.e] + kBKS - 1) / kBKS;  // stages holding the expert's rows
     // the last stage's rows past the count are zero padding or other experts' rows:
     // its MMAs stop at the last 16-row slice that holds a row of this expert
-    t.klast = (a.counts[t.e] - (t.kt - 1) * BKS + 15) / 16;
+    t.klast = (a.counts[t.e] - (t.kt - 1) * kBKS + 15) / 16;
     return t;
   }
   // ragged M: "units" are 128-row tiles (single) or pairs of them (pair mode);
@@ -219,7 +222,7 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap *tmA, const CUtens
   }
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
 // One epilogue warp's two staging buffers, used as a ring: each staged output chunk
 // (32 rows x 32 columns) takes the next buffer once the bulk store that last read it
@@ -502,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bar_pair = kPair ? mapa_shared(&full_bar[s], 0) : 0;
           if (issued != a.withhold_kblock) {
 #pragma unroll
-            for (int j = 0; j < kSub; ++j) {
+            for (int j = 0; j < Cfg<PAIR>::kSub; ++j) {
               uint8_t *sj = sA + j * Cfg<PAIR>::kSubBytes;
               issue_loads<KIND, PAIR>(&tmA, &tmB, sj, sj + kABytes, &full_bar[s], bar_pair, t,
-                                      kb * kSub + j, rank);
+                                      kb * Cfg<PAIR>::kSub + j, rank);
             }
           }
           ++issued;
@@ -561,9 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const int nk = (kb == t.kt - 1) ? t.klast : BKS / 16;
+            const int nk = (kb == t.kt - 1) ? t.klast : Cfg<PAIR>::kBKS / 16;
 #pragma unroll
-            for (int j = 0; j < kSub; ++j) {
+            for (int j = 0; j < Cfg<PAIR>::kSub; ++j) {
               const uint32_t a_addr = smem_base + s * kStageBytes + j * Cfg<PAIR>::kSubBytes;
               const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
@@ -744,11 +747,13 @@ cudaError_t launch_kind(bool pair, const CUtensorMap &tmA, const CUtensorMap &tm
               : launch_kind_as<KIND, false>(tmA, tmB, tmO, tmO2, a, max_tiles, name, st);
 }
 
-// K extent of a ragged-M GEMM: its stages of BKS and the 16-wide slices of the last one
-// that hold columns (the MMAs past them would only add the TMA's zero fill).
-void set_k(Args &a, int64_t K) {
-  a.k_tiles = cdiv(K, BKS);
-  a.k_last = cdiv(K - (int64_t)(a.k_tiles - 1) * BKS, 16);
+// K extent of a ragged-M GEMM: its stages (of the form's K per stage) and the 16-wide
+// slices of the last one that hold columns (the MMAs past them would only add the
+// TMA's zero fill).
+void set_k(Args &a, int64_t K, bool pair) {
+  const int bks = pair ? Cfg<true>::kBKS : Cfg<false>::kBKS;
+  a.k_tiles = cdiv(K, bks);
+  a.k_last = cdiv(K - (int64_t)(a.k_tiles - 1) * bks, 16);
 }
 
 Args base_args(const GemmPlan &p, int *status) {
@@ -825,13 +830,13 @@ cudaError_t gemm_gate_up(const GemmPlan &p, const void *xp, const void *w_gu, vo
   if (e != cudaSuccess) return e;
   e = gu ? map_halves(&tO2, gu, f, p.R) : map2d(&tO2, h, f, p.R, 32, 32, 64);
   if (e != cudaSuccess) return e;
+  const bool pair = pair_for_rows(p);
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN / 2);
-  set_k(a, d);
+  set_k(a, d, pair);
   a.N_out = f;
   a.f = f;
   a.out2 = gu;
-  const bool pair = pair_for_rows(p);
   return launch_kind<GATE_UP>(pair, tA, tB, tO, tO2, a, max_units(p, pair) * a.n_tiles,
                               "gemm_gate_up_swiglu", st);
 }
@@ -845,11 +850,11 @@ cudaError_t gemm_down(const GemmPlan &p, const void *h, const void *w_down, void
   if (e != cudaSuccess) return e;
   e = map2d(&tO, o, d, p.R, 32, 32, 64);
   if (e != cudaSuccess) return e;
+  const bool pair = pair_for_rows(p);
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
-  set_k(a, f);
+  set_k(a, f, pair);
   a.N_out = d;
-  const bool pair = pair_for_rows(p);
   return launch_kind<DOWN>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles, "gemm_down",
                            st);
 }
@@ -867,7 +872,7 @@ cudaError_t gemm_dgrad_h(const GemmPlan &p, const void *g, const void *w_down, c
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(f, BN);
-  set_k(a, d);
+  set_k(a, d, pair);
   a.N_out = f;
   a.f = f;
   a.aux = gu;
@@ -889,7 +894,7 @@ cudaError_t gemm_dgrad_x(const GemmPlan &p, const void *dgu, const void *w_gu, v
   if (e != cudaSuccess) return e;
   Args a = base_args(p, status);
   a.n_tiles = cdiv(d, BN);
-  set_k(a, 2 * (int64_t)f);
+  set_k(a, 2 * (int64_t)f, pair);
   a.N_out = d;
   return launch_kind<DGRAD_X>(pair, tA, tB, tO, tO, a, max_units(p, pair) * a.n_tiles,
                               "gemm_dgrad_x", st);
