@@ -264,7 +264,10 @@ __global__ void __launch_bounds__(256) scatter_kernel(
 // y[t] = sum_j w[t][j] * o[row_of[t][j]], fp32 FMA in slot order, one bf16 rounding.
 // With unit weights it is the backward's dX gather-sum. Several warps per row shorten
 // each warp's chain of dependent row loads (the kernel is latency-bound below ~1 GB).
-template <bool WEIGHTED, int WPT>
+// KT > 0 (k <= KT): the k row loads of a vector are all issued before the sum uses
+// them (measured on GB300: 15-23% faster than loading inside the sum at k = 4);
+// KT = 0: any k <= 16, each load consumed as it arrives.
+template <bool WEIGHTED, int WPT, int KT>
 __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict__ o,
                                                          const float *__restrict__ w,
                                                          const int32_t *__restrict__ row_of,
@@ -291,13 +294,31 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (KT > 0) {
+      uint4 raw[KT > 0 ? KT : 1];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k) {
-        float f[8];
-        unpack8(__ldg(o + (int64_t)rows[j] * nvec + v), f);
+      for (int j = 0; j < KT; ++j)
+        if (j < k) raw[j] = __ldg(o + (int64_t)rows[j] * nvec + v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = WEIGHTED ? fmaf(wts[j], f[i], acc[i]) : acc[i] + f[i];
+      for (int j = 0; j < KT; ++j) {
+        if (j < k) {
+          float f[8];
+          unpack8(raw[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            acc[i] = WEIGHTED ? fmaf(wts[j], f[i], acc[i]) : acc[i] + f[i];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          float f[8];
+          unpack8(__ldg(o + (int64_t)rows[j] * nvec + v), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            acc[i] = WEIGHTED ? fmaf(wts[j], f[i], acc[i]) : acc[i] + f[i];
+        }
       }
     }
     y[(int64_t)t * nvec + v] = pack8(acc);
@@ -540,18 +561,26 @@ cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *ran
 }
 
 // warps per token of the gather kernels: more for longer rows (at least 64 vectors each)
+template <bool WEIGHTED, int KT>
+static void launch_gather_kt(const void *o, const float *w, const int32_t *row_of, void *y,
+                             int T, int nvec, int k, cudaStream_t st) {
+  if (nvec >= 256)
+    gather_sum_kernel<WEIGHTED, 4, KT><<<ceil_div(T, 2), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+  else if (nvec >= 128)
+    gather_sum_kernel<WEIGHTED, 2, KT><<<ceil_div(T, 4), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+  else
+    gather_sum_kernel<WEIGHTED, 1, KT><<<ceil_div(T, 8), 256, 0, st>>>(
+        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+}
+
 template <bool WEIGHTED>
 static void launch_gather(const void *o, const float *w, const int32_t *row_of, void *y, int T,
                           int nvec, int k, cudaStream_t st) {
-  if (nvec >= 256)
-    gather_sum_kernel<WEIGHTED, 4><<<ceil_div(T, 2), 256, 0, st>>>(
-        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
-  else if (nvec >= 128)
-    gather_sum_kernel<WEIGHTED, 2><<<ceil_div(T, 4), 256, 0, st>>>(
-        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
-  else
-    gather_sum_kernel<WEIGHTED, 1><<<ceil_div(T, 8), 256, 0, st>>>(
-        (const uint4 *)o, w, row_of, (uint4 *)y, T, nvec, k);
+  if (k <= 4) launch_gather_kt<WEIGHTED, 4>(o, w, row_of, y, T, nvec, k, st);
+  else if (k <= 8) launch_gather_kt<WEIGHTED, 8>(o, w, row_of, y, T, nvec, k, st);
+  else launch_gather_kt<WEIGHTED, 0>(o, w, row_of, y, T, nvec, k, st);
 }
 
 cudaError_t launch_combine(const void *o, const float *w, const int32_t *row_of, void *y, int T,
