@@ -54,6 +54,7 @@ FFN_CASES = [
     (900, 200, 3, 2, 200, 18, False),
     (300, 64, 256, 16, 64, 19, False),   # the largest E and k: 256 experts of ~19 rows
     (200, 64, 4, 2, 24, 20, False),      # f = 24: gate and up N tiles of 24 columns
+    (300, 2048, 16, 6, 64, 21, False),   # combine: 4 warps per row, k = 6 (loads staged for k <= 8)
 ]
 
 
@@ -167,6 +168,7 @@ BWD_CASES = [
     (1024, 384, 4, 2, 576, 48, False),   # pairs with N tails in every GEMM (384, 576, 1152)
     (300, 64, 256, 16, 64, 49, False),   # the largest E and k
     (333, 72, 3, 2, 40, 50, False),      # K tail of 8 (d = 72) and N tails of 40 (f = 40)
+    (600, 1536, 8, 4, 128, 51, False),   # combine and dX gather: 2 warps per row (d = 1536)
 ]
 
 
