@@ -33,7 +33,7 @@ namespace {
 // Pair: two SMs (a 2-CTA cluster) share one 256 x 256 tile through the cta_group::2
 // MMA: each CTA loads its own 128 rows of A and half of the B tile, the even CTA
 // issues the MMA, and each CTA keeps its 128 rows of the accumulator in its TMEM. Per
-// CTA a k-block then moves 32 KB instead of 48 KB, which leaves room for 6 stages.
+// CTA a k-block then moves 32 KB instead of 48 KB, which leaves room for 6 K-blocks in flight.
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 
