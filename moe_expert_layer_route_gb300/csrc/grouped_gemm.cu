@@ -105,6 +105,7 @@ struct Args {
 // feed the MMA but nothing is stored).
 struct Tile {
   int e, m0, n0, kt, kr0;
+  int n;      // accumulator columns (the MMA's N): BN, or BN / split in a split last wave
   int klast;  // 16-wide K slices of the last stage that hold data (at most 4 * kSub)
   bool valid;
 };
@@ -116,11 +117,47 @@ __device__ __forceinline__ int total_tiles(const Args &a) {
   return (a.padded[a.E] / BM) * a.n_tiles;
 }
 
+// The last wave of a pair launch of DGRAD_H: when the tiles do not fill the final
+// round of the persistent loop, the tiles of that round (from `first` on) are cut into
+// `split` narrower tiles along N (the MMA's N = BN / split; each CTA of the pair takes
+// N / 2 of its K-major B rows), so the round runs on more pairs. Measured on GB300 at
+// gpt_oss_20b: dgrad_h 269 -> 263 us; the same split left down and dgrad_x unchanged
+// (a narrow tile still pays the full per-stage barrier cost), so it is not used there.
+struct Tail {
+  int first;  // tiles before the split round
+  int split;  // 1, 2 or 4
+};
+
 template <int KIND, bool PAIR>
-__device__ __forceinline__ Tile decode(const Args &a, int tile, int rank) {
+__device__ __forceinline__ Tail tail_split(int total, int pairs) {
+  Tail tl{total, 1};
+  if (!PAIR || KIND != DGRAD_H) return tl;
+  const int rem = total % pairs;
+  if (rem == 0) return tl;
+  tl.split = 4 * rem <= pairs ? 4 : (2 * rem <= pairs ? 2 : 1);
+  tl.first = total - rem;
+  return tl;
+}
+
+template <int KIND, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const Args &a, int tile, int rank);
+
+template <int KIND, bool PAIR>
+__device__ __forceinline__ Tile decode(const Args &a, const Tail &tl, int tile, int rank) {
+  if (tile < tl.first || tl.split == 1) return decode_tile<KIND, PAIR>(a, tile, rank);
+  const int sub = tile - tl.first;
+  Tile t = decode_tile<KIND, PAIR>(a, tl.first + sub / tl.split, rank);
+  t.n = BN / tl.split;
+  t.n0 += (sub % tl.split) * t.n;
+  return t;
+}
+
+template <int KIND, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const Args &a, int tile, int rank) {
   constexpr int kMTile = Cfg<PAIR>::kMTile;
   Tile t;
   t.valid = true;
+  t.n = BN;
   t.klast = Cfg<PAIR>::kBKS / 16;
   if (KIND == WGRAD) {
     const int per = a.m_tiles * a.n_tiles;
@@ -210,11 +247,13 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap *tmA, const CUtens
       for (int i = 0; i < 4; ++i) ld4(sB + i * kBoxBytes, tmB, t.n0 + 64 * (i & 1), i >> 1, k0, t.e);
     }
   } else if (KIND == DOWN) {
-    const int n_lo = t.n0 + rank * kBRows;
+    // a pair's MMA takes N / 2 B columns from each CTA (N = t.n)
+    const int n_lo = t.n0 + rank * (kPair ? t.n / 2 : 0);
 #pragma unroll
     for (int i = 0; i < kBRows / 64; ++i) ld3(sB + i * kBoxBytes, tmB, n_lo + 64 * i, k0, t.e);
   } else if (KIND == DGRAD_H || KIND == DGRAD_X) {
-    ld3(sB, tmB, k0, t.n0 + rank * kBRows, t.e);  // kBRows N-rows x 64 K, K-major
+    // kBRows N-rows x 64 K, K-major; the MMA uses the first N / 2 of each CTA's rows
+    ld3(sB, tmB, k0, t.n0 + rank * (kPair ? t.n / 2 : 0), t.e);
   } else {
     const int n_lo = t.n0 + rank * kBRows;
 #pragma unroll
@@ -337,7 +376,8 @@ __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int col = t.n0 + ch * 128 + 32 * c;
-      const bool ok = col < a.N_out && (KIND != WGRAD || row0 < a.M_out);
+      const bool ok = col < a.N_out && ch * 128 + 32 * c < t.n &&
+                      (KIND != WGRAD || row0 < a.M_out);
       if (ok) {
         if (KIND == WGRAD) {
           const int cw[3] = {col, row0, t.e};
@@ -368,7 +408,8 @@ __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint
         }
       }
     };
-    const int c_begin = ch * 128, c_end = ch * 128 + 128;
+    const int c_begin = ch * 128, c_end = min(ch * 128 + 128, t.n);
+    if (c_begin >= c_end) return false;  // a narrow last-wave tile: no columns here
     load(t.n0 + c_begin, cg, cu);
 #pragma unroll 1
     for (int c32 = c_begin; c32 < c_end; c32 += 32) {
@@ -414,7 +455,7 @@ __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint
 // gate/up values for the tile's columns into L2, so the epilogue's loads hit L2.
 __device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, int row, int ch) {
   const char *base = reinterpret_cast<const char *>(a.aux) + (int64_t)row * a.ld_aux * 2;
-  const int c_end = min(t.n0 + ch * 128 + 128, a.f);
+  const int c_end = min(t.n0 + min(ch * 128 + 128, t.n), a.f);
 #pragma unroll 1
   for (int c = t.n0 + ch * 128; c < c_end; c += 64) {  // 64 bf16 = one 128-byte line
     asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 2 * (int64_t)c));
@@ -483,7 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kPair) cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
-  const int total = total_tiles<KIND, PAIR>(a);
+  const int full = total_tiles<KIND, PAIR>(a);
+  const Tail tl = tail_split<KIND, PAIR>(full, units);
+  const int total = tl.first + (full - tl.first) * tl.split;
   bool failed = false;
 
   if (warp == 0) {
@@ -494,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;
       for (int tile = unit0; tile < total && ok; tile += units) {
-        const Tile t = decode<KIND, PAIR>(a, tile, rank);
+        const Tile t = decode<KIND, PAIR>(a, tl, tile, rank);
         for (int kb = 0; kb < t.kt; ++kb) {
           if (!mbar_wait(&empty_bar[s], ph ^ 1, a.status, a.wait_ns)) {
             ok = false;
@@ -546,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, any = false;
       const uint32_t smem_base = smem_u32(smem);
       for (int tile = unit0; tile < total && ok; tile += units) {
-        const Tile t = decode<KIND, PAIR>(a, tile, 0);
+        const Tile t = decode<KIND, PAIR>(a, tl, tile, 0);
+        const uint32_t idesc = t.n == BN ? kIdesc : idesc_bf16_f32(kMTile, t.n, A_MN, B_MN);
         if (!mbar_wait(&acce_bar[buf], aph ^ 1, a.status, a.wait_ns)) {
           ok = false;
           break;
@@ -575,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint64_t ad = smem_desc_sw128(a_addr + kk * kAStep, kALbo, 1024);
                   const uint64_t bd = smem_desc_sw128(b_addr + kk * kBStep, kBLbo, 1024);
                   const uint32_t acc = (kb | j | kk) != 0;
-                  if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, acc);
-                  else tc_mma_bf16(d_tmem, ad, bd, kIdesc, acc);
+                  if (kPair) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                  else tc_mma_bf16(d_tmem, ad, bd, idesc, acc);
                 }
               }
             }
@@ -615,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int buf = 0;
     uint32_t aph = 0;
     for (int tile = unit0; tile < total; tile += units) {
-      const Tile t = decode<KIND, PAIR>(a, tile, rank);
+      const Tile t = decode<KIND, PAIR>(a, tl, tile, rank);
       if (KIND == DGRAD_H && t.valid) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
       bool ok = mbar_wait(&accf_bar[buf], aph, a.status, a.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
