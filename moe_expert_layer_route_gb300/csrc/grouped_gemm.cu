@@ -4,9 +4,9 @@
 // integration": grouped GEMM with a fused SwiGLU; "One trainer architecture": fused
 // experts as 3-D weight tensors) run as one persistent kernel per GEMM over all
 // experts. Design:
-//   * one CTA per SM, 320 threads: warp 0 issues TMA loads, warp 1 issues tcgen05.mma
-//     (one elected lane), warps 2..9 run the epilogue out of TMEM (two per TMEM lane
-//     quarter, each on half of the tile's columns);
+//   * one CTA per SM: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one elected
+//     lane), the other warps run the epilogue out of TMEM (per kind 8, two per TMEM lane
+//     quarter each on half of the tile's columns, or 4, one per quarter);
 //   * two forms: a CTA alone on a 128 x 256 (M x N) tile, or a 2-CTA cluster on a
 //     256 x 256 tile through the cta_group::2 MMA (each CTA loads its 128 A rows and
 //     half of B, the even CTA issues the MMAs);
@@ -54,8 +54,7 @@ struct Cfg {
   static constexpr int kStageBytes = kSub * kSubBytes;
 };
 constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box (MN-major tiles are built of these)
-constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of the columns
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 8;  // at most: two per TMEM lane quarter, each on half of the columns
 constexpr int kTmemCols = 512;
 // epilogue staging: per epilogue warp two 32-row x 32-column bf16 buffers (2 KB each,
 // 64-byte swizzled like the TMA store expects)
@@ -75,6 +74,20 @@ constexpr int64_t kPairMinRows = 384;
 constexpr int64_t kWeightStationaryMaxRows = 2048;
 
 enum Kind { GATE_UP = 0, DOWN = 1, DGRAD_H = 2, DGRAD_X = 3, WGRAD = 4 };
+
+// Epilogue warps of a kind: 8 (two per TMEM lane quarter, each on half of the tile's
+// columns) or 4 (one per quarter, both halves in turn). Four leave fewer warps beside
+// the producer and MMA lanes on their SMSPs; measured on GB300 at gpt_oss_20b they made
+// gate_up, down and dgrad_x 3-5 us faster each, but wgrad_down slower and dgrad_h (whose
+// SwiGLU-backward epilogue is the heaviest) 60 us slower.
+template <int KIND>
+constexpr int epi_warps() {
+  return (KIND == GATE_UP || KIND == DOWN || KIND == DGRAD_X) ? 4 : 8;
+}
+template <int KIND>
+constexpr int threads_of() {
+  return 64 + 32 * epi_warps<KIND>();
+}
 
 struct Args {
   const int32_t *padded;       // [E+1]
@@ -336,6 +349,7 @@ __device__ __forceinline__ void release_acc(int lane, uint64_t *bar_local, uint3
 // Returns whether it released the accumulator.
 template <int KIND>
 __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint32_t taddr,
+                                              bool last_half,
                                               int q, int ch, int lane, Stager &st,
                                               const CUtensorMap *tmO, const CUtensorMap *tmO2,
                                               uint64_t *rel_local, uint32_t rel_pair,
@@ -345,8 +359,8 @@ __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint
     // accumulator columns [0,128) gate, [128,256) up; this warp: h columns ch*64 ..+63
     float g[64], u[64];
     tmem_ld64x2(taddr + ch * 64, taddr + BN / 2 + ch * 64, g, u);
-    release_acc(lane, rel_local, rel_pair, pair);
-    if (!t.valid) return true;
+    if (last_half) release_acc(lane, rel_local, rel_pair, pair);
+    if (!t.valid) return last_half;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int col = t.n0 + ch * 64 + 32 * c;
@@ -371,8 +385,8 @@ __device__ __forceinline__ bool epilogue_tile(const Args &a, const Tile &t, uint
     } else {
       tmem_ld128(taddr + ch * 128, x);
     }
-    release_acc(lane, rel_local, rel_pair, pair);
-    if (!t.valid) return true;
+    if (last_half) release_acc(lane, rel_local, rel_pair, pair);
+    if (!t.valid) return last_half;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int col = t.n0 + ch * 128 + 32 * c;
@@ -465,7 +479,7 @@ __device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, in
 
 // Launched with a cluster of 2 when PAIR (see launch_kind).
 template <int KIND, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<KIND>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO,
@@ -500,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 1);
-      mbar_init(&acce_bar[b], kPair ? 2 * kEpiWarps : kEpiWarps);  // both CTAs' epilogues
+      mbar_init(&acce_bar[b], (kPair ? 2 : 1) * epi_warps<KIND>());  // both CTAs' epilogues
     }
     mbar_init(&drain_bar, 1);
     fence_barrier_init();
@@ -652,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------------- epilogue
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int ch = (warp - 2) >> 2;  // which half of the tile's columns it handles
+    // which half of the tile's columns it handles (-1: both, one after the other)
+    const int ch_own = epi_warps<KIND>() == 8 ? (warp - 2) >> 2 : -1;
     Stager st{smem + kStages * kStageBytes + (warp - 2) * 2 * kStageOutBytes, 0};
     const uint32_t acce_pair0 = kPair ? mapa_shared(&acce_bar[0], 0) : 0;
     const uint32_t acce_pair1 = kPair ? mapa_shared(&acce_bar[1], 0) : 0;
@@ -660,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aph = 0;
     for (int tile = unit0; tile < total; tile += units) {
       const Tile t = decode<KIND, PAIR>(a, tl, tile, rank);
-      if (KIND == DGRAD_H && t.valid) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch);
+      if (KIND == DGRAD_H && t.valid) prefetch_gu_row(a, t, t.m0 + 32 * q + lane, ch_own);
       bool ok = mbar_wait(&accf_bar[buf], aph, a.status, a.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -669,9 +684,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
-      const bool released =
-          epilogue_tile<KIND>(a, t, taddr, q, ch, lane, st, &tmO, &tmO2, &acce_bar[buf],
-                              buf ? acce_pair1 : acce_pair0, kPair);
+      bool released = false;
+      for (int ch = ch_own < 0 ? 0 : ch_own; ch < (ch_own < 0 ? 2 : ch_own + 1); ++ch)
+        released = epilogue_tile<KIND>(a, t, taddr, ch_own >= 0 || ch == 1, q, ch, lane, st,
+                                       &tmO, &tmO2, &acce_bar[buf],
+                                       buf ? acce_pair1 : acce_pair0, kPair);
       if (!released) release_acc(lane, &acce_bar[buf], buf ? acce_pair1 : acce_pair0, kPair);
       buf ^= 1;
       if (buf == 0) aph ^= 1;
@@ -721,7 +738,7 @@ cudaError_t launch_kind_as(const CUtensorMap &tmA, const CUtensorMap &tmB, const
   attr.val.clusterDim.x = PAIR ? 2 : 1;
   attr.val.clusterDim.y = 1;
   attr.val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of<KIND>(), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes<PAIR>();
   cfg.stream = st;
   cfg.attrs = &attr;
