@@ -5,16 +5,21 @@
 
 One step is one pass of the whole block over one batch: route, dispatch,
 gate_up GEMM + SwiGLU, down GEMM, combine, then the backward (G scatter, dH GEMM +
-SwiGLU backward, dW_down, dXp GEMM, dW_gu, dX gather), through the C ABI on the
-gpt-oss-20b-like workload (T=4096 tokens, d=2880, E=32 experts, k=4, f=2880,
-seed 2; synthetic inputs). Rank 0 prints one JSON line.
+SwiGLU backward, dW_down, dXp GEMM, dW_gu, dX gather), through the C ABI. The
+headline workload is the largest single-GPU configuration, the long-sequence
+gpt-oss-20b-like block (T=65536 tokens, d=2880, E=32 experts, k=4, f=2880, seed 4;
+synthetic inputs); the other four seeded configurations (tiny, Qwen3-MoE-like,
+gpt-oss-20b-like, skewed load) are measured the same way and reported in the
+line's `workloads` record. Rank 0 prints one JSON line.
 
   value     tokens/s over all ranks, device-timed with CUDA events (L2 flushed
             before every timed step, outside the timed events)
   e2e       the same through the Python API with pinned host inputs copied in and
-            Y and dX copied out inside the timed region
+            Y and dX copied out inside the timed region (uploads and downloads on
+            two copy streams)
   roofline  the dominant kernel (largest share of step time): algorithmic work
-            per launch / its mean launch time from library-recorded CUDA events
+            per launch / its mean launch time from library-recorded CUDA events,
+            against the measured burst bf16 peak (or the HBM copy rate)
   cpu_baseline  the CPU oracle timed on the host cores on a bounded token sample
   --impl reference  times the CPU oracle alone (rank 0), as the reference arm.
 
@@ -44,7 +49,9 @@ import workloads  # noqa: E402
 
 METRIC = "MoE layer tokens/s and grouped-GEMM TFLOPS (% of GB300 bf16 peak), 1 GPU"
 UNIT = "tokens/s"
-WORKLOAD = "gpt_oss_20b"
+WORKLOAD = "long"     # the largest single-GPU configuration (T=65536, forward+backward)
+WORKLOAD_ORDER = ("tiny", "qwen3_moe", "gpt_oss_20b", "skewed", "long")
+NOMINAL_BF16_TFLOPS = 2250.0     # GB300 dense bf16, nominal (context beside the measured peak)
 L2_FLUSH_BYTES = 256 << 20       # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_SOURCES = ("moe_expert_layer_route_gb300/csrc/grouped_gemm.cu",
@@ -278,16 +285,17 @@ def workload_of(args) -> workloads.Workload:
     return wl
 
 
-def run_ours(args, rank, world, local_rank) -> dict | None:
-    import moe_expert_layer_route_gb300 as moe
-    from moe_expert_layer_route_gb300 import _build
-    if rank == 0 or not _build.up_to_date():
-        if world == 1 or local_rank == 0:
-            _build.build()
-    barrier(world)
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = workload_of(args)
+def gpu_index_of(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    return int(vis) if vis.isdigit() else local_rank
+
+
+def measure(moe, wl: workloads.Workload, args, K: int, W: int, world: int, dev,
+            flush: torch.Tensor, want_graph: bool, want_e2e: bool) -> dict:
+    """Device-timed, profiled, graph-replayed and end-to-end steps of one workload.
+
+    A step is one pass of the whole block (forward, and the backward when the workload
+    has one) over one batch through the C ABI. Returns the measurements as a dict."""
     inp = workloads.make_inputs(wl, with_dy=True)
     x, logits = inp.x.to(dev), inp.logits.to(dev)
     w_router = workloads.make_router_weight(wl).to(dev) if args.router_gemm else None
@@ -303,10 +311,9 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     dlogits = torch.empty_like(logits) if router_grad else None
     sel_bias = torch.from_numpy(workloads.zipf_bias(wl.E)).to(dev) if args.selection_bias else None
     aux = torch.empty(2 * wl.E + 1, dtype=torch.float32, device=dev) if args.aux_loss else None
-    views = None
+    views = moe.workspace_views(s, wl.backward, ws)
     r_scratch = torch.empty(max(16, moe.lib().moe_router_backward_scratch_size(s)),
                             dtype=torch.uint8, device=dev) if w_router is not None else None
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def run_step(x, logits, dy, y, dx):
         """One step through the library on the given input and output tensors (the
@@ -328,9 +335,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     def step():
         run_step(x, logits, dy, y, grads[0])
 
-    views = moe.workspace_views(s, wl.backward, ws)
-
-    for _ in range(args.warmup):
+    for _ in range(W):
         step()
     torch.cuda.synchronize()
     moe.check_device_status(ws)
@@ -338,15 +343,12 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
 
     # ---- device-timed region (no instrumentation inside: the library's per-launch
     # events of the profiled pass below would add their own gaps to the step)
-    K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
     launches0 = moe.launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(gpu_index) as clk:
+    with ClockSampler(gpu_index_of(dev.index or 0)) as clk:
         for i in range(K):
             flush.zero_()
             starts[i].record()
@@ -378,6 +380,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         per.setdefault(name, []).append(t)
     work = kernel_work(wl)
     pk, peak_src = peaks()
+    bf16_peak = pk["bf16_tflops"]
     stages = {}
     # a launch the library ran on its side stream beside others is named "<kernel>
     # (overlapped)": its events span the kernels it overlaps, so it takes no share and
@@ -395,7 +398,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         if amount:
             if kind == "flop":
                 entry.update(achieved=amount / (mean * 1e-3) / 1e12, unit="TFLOP/s",
-                             frac=amount / (mean * 1e-3) / 1e12 / pk["bf16_tflops_sustained"])
+                             frac=amount / (mean * 1e-3) / 1e12 / bf16_peak)
             elif kind == "alu_flop":
                 entry.update(achieved=amount / (mean * 1e-3) / 1e12, unit="TFLOP/s fp32",
                              frac=amount / (mean * 1e-3) / 1e12 / FP32_ALU_TFLOPS)
@@ -417,19 +420,20 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
             traffic = tr.get("bytes_per_launch")
     if dkind == "flop":
         ach = damount / (dmean * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"],
+        roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": ach / bf16_peak,
                 "traffic": traffic, "kernel": dom,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+                "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)",
+                "frac_of_nominal_dense": ach / NOMINAL_BF16_TFLOPS}
     else:
         ach = damount / (dmean * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"], "traffic": traffic, "kernel": dom,
-                "peak_source": f"{peak_src} hbm_gbs"}
+                "peak_source": f"{peak_src} hbm_gbs (copy)"}
     gemm_names = [n for n in per if n.startswith("gemm")]
     gemm_flop = sum(work[n][1] * len(per[n]) for n in gemm_names) / K
     gemm_ms = sum(sum(per[n]) for n in gemm_names) / K
-    gemm_tflops = gemm_flop / (gemm_ms * 1e-3) / 1e12
+    gemm_tflops = gemm_flop / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else 0.0
     # the whole step against its roofline: the slower of its FLOPs at the bf16 peak and
     # its algorithmic bytes (every stage's, GEMMs included) at the HBM copy rate
     gb = gemm_bytes(wl, wl.backward)
@@ -438,7 +442,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         kind, amount = work.get(n, ("byte", 0))
         step_bytes += (gb[n] if n in gb else amount if kind == "byte" else 0) * len(ts)
     step_bytes /= K
-    t_flop = gemm_flop / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    t_flop = gemm_flop / (bf16_peak * 1e12) * 1e3
     t_bytes = step_bytes / (pk["hbm_gbs"] * 1e9) * 1e3
     step_roofline = {"flop": gemm_flop, "bytes": step_bytes, "t_flop_ms": t_flop,
                      "t_bytes_ms": t_bytes, "bound": "tensor" if t_flop >= t_bytes else "hbm",
@@ -450,7 +454,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
     # ---- the same step captured once in a CUDA graph and replayed (the calls allocate
     # nothing and never synchronise, so they capture): device time without launch gaps
     graph = None
-    if not args.no_graph:
+    if want_graph:
         gstream = torch.cuda.Stream(device=dev)
         gstream.wait_stream(torch.cuda.current_stream(dev))
         cg = torch.cuda.CUDAGraph()
@@ -472,115 +476,211 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
         graph = {"ms_per_step": gms, "value": tokens_all / (gms * 1e-3), "unit": UNIT}
         del cg
 
-    # ---- end to end through the Python API with host buffers: every step uploads its
-    # inputs from pinned host memory and downloads its results. The copies run on a copy
-    # stream into and out of two device buffer sets, so step i+1's upload and step i-1's
-    # download overlap step i's kernels (events order each buffer's reuse).
     e2e = None
-    if not args.no_e2e:
-        ke = max(4, min(K, 50))
-        hx = inp.x.pin_memory()
-        hl = inp.logits.pin_memory()
-        hdy = inp.dy.pin_memory() if wl.backward else None
-        hy = [torch.empty_like(hx).pin_memory() for _ in range(2)]
-        hdx = [torch.empty_like(hx).pin_memory() for _ in range(2)] if wl.backward else None
-        dsets = [(torch.empty_like(x), torch.empty_like(logits),
-                  torch.empty_like(dy) if wl.backward else None, torch.empty_like(x),
-                  torch.empty_like(x) if wl.backward else None) for _ in range(2)]
-        comp = torch.cuda.current_stream(dev)
-        copy = torch.cuda.Stream(device=dev)
-        loaded = [torch.cuda.Event() for _ in range(2)]     # inputs of a set are on the device
-        computed = [torch.cuda.Event() for _ in range(2)]   # the set's step has run
+    if want_e2e:
+        e2e = measure_e2e(wl, inp, run_step, x, logits, dy, w_router is not None, K, world,
+                          dev, tokens_all)
+    return {"wl": wl, "ms": ms, "value": tokens_all / (ms * 1e-3),
+            "ms_median": statistics.median(step_ms), "stages": stages, "roofline": roof,
+            "gemm_tflops": gemm_tflops, "gemm_flop": gemm_flop, "step_roofline": step_roofline,
+            "experts": experts, "graph": graph, "e2e": e2e, "launches": launches,
+            "clocks": clk.summary(), "router_grad": router_grad,
+            "w_router": None if w_router is None else w_router.cpu(), "inp": inp}
 
-        def upload(i):
-            bx, bl, bdy, _, _ = dsets[i % 2]
-            with torch.cuda.stream(copy):
-                # (the set's previous download, on this stream, came first)
-                bx.copy_(hx, non_blocking=True)
-                if w_router is None:
-                    bl.copy_(hl, non_blocking=True)
-                if wl.backward:
-                    bdy.copy_(hdy, non_blocking=True)
-                loaded[i % 2].record(copy)
 
-        def compute(i):
-            bx, bl, bdy, by, bdx = dsets[i % 2]
-            comp.wait_event(loaded[i % 2])
-            run_step(bx, bl, bdy, by, bdx)
-            computed[i % 2].record(comp)
+def measure_e2e(wl, inp, run_step, x, logits, dy, router_gemm: bool, K: int, world: int, dev,
+                tokens_all: float) -> dict:
+    """End to end through the Python API with host buffers: every step uploads its inputs
+    from pinned host memory and downloads its results (Y, and dX when the workload has a
+    backward). Uploads run on one copy stream and downloads on another, so the two
+    directions overlap each other and the kernels; three device buffer sets let step i+1's
+    upload and step i-1's download run beside step i (events order each set's reuse)."""
+    nset = 3
+    ke = max(4, min(K, 50))
+    hx = inp.x.pin_memory()
+    hl = inp.logits.pin_memory()
+    hdy = inp.dy.pin_memory() if wl.backward else None
+    hy = [torch.empty_like(hx).pin_memory() for _ in range(nset)]
+    hdx = [torch.empty_like(hx).pin_memory() for _ in range(nset)] if wl.backward else None
+    dsets = [(torch.empty_like(x), torch.empty_like(logits),
+              torch.empty_like(dy) if wl.backward else None, torch.empty_like(x),
+              torch.empty_like(x) if wl.backward else None) for _ in range(nset)]
+    comp = torch.cuda.current_stream(dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+    loaded = [torch.cuda.Event() for _ in range(nset)]      # the set's inputs are on the device
+    computed = [torch.cuda.Event() for _ in range(nset)]    # the set's step has run
+    drained = [torch.cuda.Event() for _ in range(nset)]     # the set's results are on the host
+    used = [False] * nset
 
-        def download(i):
-            _, _, _, by, bdx = dsets[i % 2]
-            with torch.cuda.stream(copy):
-                copy.wait_event(computed[i % 2])
-                hy[i % 2].copy_(by, non_blocking=True)
-                if wl.backward:
-                    hdx[i % 2].copy_(bdx, non_blocking=True)
+    def upload(i):
+        b = i % nset
+        bx, bl, bdy, _, _ = dsets[b]
+        with torch.cuda.stream(up):
+            if used[b]:
+                up.wait_event(computed[b])      # the set's previous step read its inputs
+            bx.copy_(hx, non_blocking=True)
+            if not router_gemm:
+                bl.copy_(hl, non_blocking=True)
+            if wl.backward:
+                bdy.copy_(hdy, non_blocking=True)
+            loaded[b].record(up)
 
-        def run(n):
-            upload(0)
-            for i in range(n):
-                if i + 1 < n:
-                    upload(i + 1)       # the set of step i+1 was drained after step i-1
-                compute(i)
-                download(i)
+    def compute(i):
+        b = i % nset
+        bx, bl, bdy, by, bdx = dsets[b]
+        comp.wait_event(loaded[b])
+        if used[b]:
+            comp.wait_event(drained[b])         # the set's previous results have left
+        run_step(bx, bl, bdy, by, bdx)
+        computed[b].record(comp)
+        used[b] = True
 
-        run(3)
+    def download(i):
+        b = i % nset
+        _, _, _, by, bdx = dsets[b]
+        with torch.cuda.stream(down):
+            down.wait_event(computed[b])
+            hy[b].copy_(by, non_blocking=True)
+            if wl.backward:
+                hdx[b].copy_(bdx, non_blocking=True)
+            drained[b].record(down)
+
+    def run(n):
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            compute(i)
+            download(i)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(comp)
+    up.wait_event(ev0)
+    down.wait_event(ev0)
+    run(ke)
+    comp.wait_stream(down)          # the last download is part of the timed region
+    ev1.record(comp)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) * 1e3 / ke
+    e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
+    h2d = hx.numel() * 2 + (hl.numel() * 4 if not router_gemm else 0) + \
+        (hdy.numel() * 2 if wl.backward else 0)
+    d2h = hx.numel() * 2 * (2 if wl.backward else 1)
+
+    # copy rates alone (no kernels beside them), for reading the e2e figure
+    def rate(fn, nbytes):
         torch.cuda.synchronize()
-        barrier(world)
-        t0 = time.perf_counter()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(comp)
-        copy.wait_event(ev0)
-        run(ke)
-        comp.wait_stream(copy)          # the last download is part of the timed region
-        ev1.record(comp)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            fn()
+        b.record()
         torch.cuda.synchronize()
-        wall = (time.perf_counter() - t0) * 1e3 / ke
-        e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
-        h2d = hx.numel() * 2 + (hl.numel() * 4 if w_router is None else 0) + \
-            (hdy.numel() * 2 if wl.backward else 0)
-        d2h = hx.numel() * 2 * (2 if wl.backward else 1)
-        e2e = {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "copies": "copy stream, two device buffer sets: uploads and downloads overlap "
-                         "the neighbouring steps' kernels"}
+        return 3 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
 
+    bx0 = dsets[0][0]
+    h2d_gbs = rate(lambda: bx0.copy_(hx, non_blocking=True), hx.numel() * 2)
+    d2h_gbs = rate(lambda: hy[0].copy_(bx0, non_blocking=True), hx.numel() * 2)
+    return {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "copy_gbs_alone": {"h2d": h2d_gbs, "d2h": d2h_gbs},
+            "copies": "uploads and downloads on two copy streams, three device buffer sets: "
+                      "both directions overlap each other and the neighbouring steps' kernels"}
+
+
+def passes_of(wl, args, router_grad: bool) -> str:
+    return (("forward+backward" if wl.backward else "forward")
+            + (" + fp32 router GEMM (logits from x)" if args.router_gemm else "")
+            + (" + router-logit gradient" if router_grad and wl.backward else "")
+            + (" + router GEMM gradient (dW_r, dX)" if args.router_gemm and router_grad
+               and wl.backward else "")
+            + (" + selection bias (Zipf)" if args.selection_bias else "")
+            + (" + load-balancing statistics and gradient" if args.aux_loss else ""))
+
+
+def summary_of(m: dict) -> dict:
+    """The figures of one workload for the line's `workloads` record."""
+    wl = m["wl"]
+    gemms = {n: {"ms": v["ms"], "tflops": v.get("achieved"), "frac": v.get("frac")}
+             for n, v in m["stages"].items() if n.startswith("gemm")}
+    bw = {n: {"ms": v["ms"], "gbs": v.get("achieved"), "frac": v.get("frac")}
+          for n, v in m["stages"].items()
+          if not n.startswith("gemm") and v.get("unit") == "GB/s"}
+    pk, _ = peaks()
+    return {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
+            "seed": wl.seed, "passes": "forward+backward" if wl.backward else "forward",
+            "value": m["value"], "unit": UNIT, "ms_per_step": m["ms"],
+            "e2e": None if m["e2e"] is None else m["e2e"]["value"],
+            "gemm_tflops": m["gemm_tflops"],
+            "gemm_frac_of_bf16_peak": m["gemm_tflops"] / pk["bf16_tflops"],
+            "step_roofline_frac": m["step_roofline"]["frac"],
+            "step_bound": m["step_roofline"]["bound"],
+            "gemms": gemms, "bandwidth_kernels": bw, "experts": m["experts"],
+            "clocks": m["clocks"]}
+
+
+def run_ours(args, rank, world, local_rank) -> dict | None:
+    import moe_expert_layer_route_gb300 as moe
+    from moe_expert_layer_route_gb300 import _build
+    if rank == 0 or not _build.up_to_date():
+        if world == 1 or local_rank == 0:
+            _build.build()
+    barrier(world)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    wl = workload_of(args)
+    head = measure(moe, wl, args, args.steps, args.warmup, world, dev, flush,
+                   want_graph=not args.no_graph, want_e2e=not args.no_e2e)
+    torch.cuda.empty_cache()
+    others = {}
+    if not args.no_workloads and args.tokens is None and args.experts is None:
+        k_sub = max(5, min(args.steps, 30))
+        for name in WORKLOAD_ORDER:
+            if name == wl.name:
+                continue
+            m = measure(moe, workloads.WORKLOADS[name], args, k_sub, args.warmup, world, dev,
+                        flush, want_graph=False, want_e2e=not args.no_e2e)
+            others[name] = summary_of(m)
+            del m
+            torch.cuda.empty_cache()
     if rank != 0:
         return None
+    pk, _ = peaks()
     out = {
-        "metric": METRIC, "value": tokens_all / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
         "config": {"workload": wl.description, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k,
                    "f": wl.f, "seed": wl.seed,
-                   "passes": ("forward+backward" if wl.backward else "forward")
-                   + (" + fp32 router GEMM (logits from x)" if args.router_gemm else "")
-                   + (" + router-logit gradient" if router_grad and wl.backward else "")
-                   + (" + router GEMM gradient (dW_r, dX)" if args.router_gemm and router_grad
-                      and wl.backward else "")
-                   + (" + selection bias (Zipf)" if args.selection_bias else "")
-                   + (" + load-balancing statistics and gradient" if args.aux_loss else ""),
+                   "passes": passes_of(wl, args, head["router_grad"]),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed (256 MB write) before each timed step, outside its events; "
                          f"weights alone are {6 * wl.E * wl.d * wl.f / 1e9:.2f} GB"},
-        "gemm_tflops": gemm_tflops,
-        "gemm_frac_of_bf16_peak": gemm_tflops / pk["bf16_tflops_sustained"],
-        "gemm_flop_per_step": gemm_flop,
-        "ms_per_step_median": statistics.median(step_ms),
-        "step_roofline": step_roofline,
-        "experts": experts,
-        "graph": graph,
-        "roofline": roof,
-        "stages": stages,
-        "gpu_launches": launches,
-        "clocks": clk.summary(),
-        "e2e": e2e,
+        "gemm_tflops": head["gemm_tflops"],
+        "gemm_frac_of_bf16_peak": head["gemm_tflops"] / pk["bf16_tflops"],
+        "gemm_frac_of_nominal_dense": head["gemm_tflops"] / NOMINAL_BF16_TFLOPS,
+        "gemm_flop_per_step": head["gemm_flop"],
+        "ms_per_step_median": head["ms_median"],
+        "step_roofline": head["step_roofline"],
+        "experts": head["experts"],
+        "graph": head["graph"],
+        "roofline": head["roofline"],
+        "stages": head["stages"],
+        "gpu_launches": head["launches"],
+        "clocks": head["clocks"],
+        "e2e": head["e2e"],
+        "workloads": others,
     }
     if not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds,
-                                           None if w_router is None else w_router.cpu())
+        out["cpu_baseline"] = cpu_baseline(wl, head["inp"], args.cpu_seconds, head["w_router"])
     return out
 
 
@@ -635,6 +735,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay timing of the step")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only the headline workload (no `workloads` record)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     ap.add_argument("--router-grad", action="store_true",

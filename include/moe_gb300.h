@@ -177,7 +177,10 @@ moe_status moe_expert_ffn(moe_shape s, const moe_bf16 *xp, const int32_t *counts
  * their token weighted by the top-k probabilities.
  *   y[t] = bf16( sum_{j=0..k-1} w[t][j] * o[row_of[t][j]] ), an fp32 sum in slot
  *   order, one rounding. A gather per token: deterministic, no atomics.
- *   o [R x d] bf16 in; w [T x k] fp32 in; row_of [T x k] int32 in; y [T x d] bf16 out. */
+ *   o [rows x d] bf16 in (any row space row_of indexes: the padded one of moe_dispatch,
+ *   or the compact one of moe_ep_dispatch); w [T x k] fp32 in, or NULL for unit
+ *   weights (the plain sum, e.g. the dX gather of an expert-parallel backward);
+ *   row_of [T x k] int32 in; y [T x d] bf16 out. */
 moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int32_t *row_of,
                        moe_bf16 *y, moe_stream stream);
 
@@ -267,6 +270,102 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
                         moe_bf16 *dw_gu, moe_bf16 *dw_down, float *dlogits, void *scratch,
                         size_t scratch_bytes, moe_stream stream);
 
+/* Backward of the experts alone (moe_expert_ffn's gradient), for a caller that forms
+ * the row gradient G itself (the expert-parallel backward: G arrives from other
+ * ranks). For every expert e and its segment rows, as in moe_backward:
+ *   dH = G W_down[e]^T;  dgate = dH * up * silu'(gate),  dup = dH * silu(gate);
+ *   dW_down[e] = H_e^T G_e;  dW_gu[e] = Xp_e^T [dgate | dup];  dXp = [dgate | dup] W_gu[e]^T
+ * on the tcgen05 tensor cores (bf16 operands, fp32 accumulation, dGU rounded to bf16
+ * as the GEMM operand, outputs rounded once). Experts with no rows get dW = 0.
+ *   g [R x d] bf16 in, segment-padded like xp with zero padding rows; xp [R x d],
+ *   gu [R x 2f], h [R x f] bf16 in (from moe_expert_ffn on the same counts);
+ *   counts [E] int32 in; w_gu, w_down as in moe_expert_ffn;
+ *   dxp [R x d] bf16 out (padding rows zero); dw_gu [E x d x 2f], dw_down [E x f x d] out;
+ *   ws: at least moe_workspace_size(s, 0) bytes (tile plan, status word);
+ *   scratch: at least moe_backward_scratch_size(s) bytes (dGU). */
+moe_status moe_expert_ffn_backward(moe_shape s, const moe_bf16 *g, const moe_bf16 *xp,
+                                   const moe_bf16 *gu, const moe_bf16 *h, const int32_t *counts,
+                                   const moe_bf16 *w_gu, const moe_bf16 *w_down, moe_bf16 *dxp,
+                                   moe_bf16 *dw_gu, moe_bf16 *dw_down, void *ws, size_t ws_bytes,
+                                   void *scratch, size_t scratch_bytes, moe_stream stream);
+
+/* ----------------------------------------------------------- expert parallelism
+ * "Halo's 2.8x over TRL is not a kernel, and its own benchmark proves it", Figure 3
+ * ("EP token routing") and section "Where the gap actually is": with the experts
+ * sharded over G ranks, tokens are sorted by expert, each row is sent to the rank
+ * that owns its expert (the dispatch all-to-all), the owners run their experts, and
+ * the rows return (the combine all-to-all) to be summed at their token, weighted by
+ * the top-k probabilities. The TorchTurbo README's expert-parallel plan shards the
+ * fused expert weights Shard(0): rank g owns experts [g E/G, (g+1) E/G), E % G == 0.
+ *
+ * One rank's forward, around the caller's two exchanges (all-to-all over the ranks,
+ * e.g. NCCL; these calls never wait on another rank):
+ *   1. moe_route, then moe_ep_dispatch: the rows sorted by expert into a compact send
+ *      buffer xs [T k x d] whose rows for rank r are [offsets[r El], offsets[(r+1) El]),
+ *      El = E / G, and counts [E] (rank r receives counts[r El .. (r+1) El)).
+ *   2. exchange the counts: recv_counts [G x El], row s from source rank s; then the
+ *      rows: xr [n_recv x d], source-major ([s][local expert][rows]).
+ *   3. moe_ep_regroup into the local segment-padded layout of the local shape
+ *      (moe_ep_local_shape), moe_expert_ffn over the El local experts, moe_ep_unregroup
+ *      back to the received order.
+ *   4. exchange the rows back (the reverse splits): ob [T k x d] in xs's order, then
+ *      moe_combine(s, ob, w, row_of, y).
+ * The backward mirrors it: moe_ep_grad_scatter (G = w dY in xs's order, and the
+ * router-logit gradient from ob), the exchange, moe_ep_regroup of G,
+ * moe_expert_ffn_backward, moe_ep_unregroup of dXp, the exchange back, and
+ * moe_combine with w = NULL (dX[t] = sum_j dXs[row_of[t][j]]). Every rank gets the
+ * complete dW of its own experts (they saw every token routed to them). */
+
+/* The local shape of rank-side expert work: E/G experts, T*G tokens (a bound on the
+ * tokens that can reach one rank when every rank holds T), min(k, E/G) experts per
+ * token; its padded row space holds every row a rank can receive. Needs E % G == 0. */
+moe_status moe_ep_local_shape(moe_shape s, int G, moe_shape *out);
+
+/* The dispatch of moe_dispatch into the compact layout of the method: xs row
+ * offsets[e] + (rank of token t among expert e's tokens) = x[t], no padding rows.
+ *   x [T x d] bf16 in; ids [T x k] int32 in; xs [T k x d] bf16 out; counts [E],
+ *   offsets [E+1] int32 out; row_of [T x k] int32 out (compact row of (t, j));
+ *   ws: at least moe_workspace_size(s, 0) bytes. */
+moe_status moe_ep_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xs,
+                           int32_t *counts, int32_t *offsets, int32_t *row_of, void *ws,
+                           size_t ws_bytes, moe_stream stream);
+
+/* Received rows to the local experts' segment-padded layout. Received row i of block
+ * (source s, local expert e) goes to row P_e + sum_{s'<s} recv_counts[s'][e] + (its
+ * index in the block), P_e = 128 * sum_{e'<e} ceil(counts_loc[e'] / 128): per expert,
+ * the sources in rank order, each in its sender's token order. Padding rows are zeroed.
+ *   s_loc: the local shape (moe_ep_local_shape); recv_counts [G x El] int32 in (device);
+ *   n_recv: the number of received rows (the sum of recv_counts), at most s_loc.T *
+ *   s_loc.k; xr [n_recv x d] bf16 in; xp [R_loc x d] bf16 out, R_loc =
+ *   moe_padded_rows(s_loc); counts_loc [El], padded_loc [El+1] int32 out;
+ *   dest_of [n_recv] int32 out (the padded row of each received row);
+ *   ws: at least moe_workspace_size(s_loc, 0) bytes. If the device counts do not add up
+ *   to n_recv (or are negative), nothing is written and moe_check_device_status(ws)
+ *   returns MOE_ERR_INVALID_ARG. */
+moe_status moe_ep_regroup(moe_shape s_loc, int G, const int32_t *recv_counts, int64_t n_recv,
+                          const moe_bf16 *xr, moe_bf16 *xp, int32_t *counts_loc,
+                          int32_t *padded_loc, int32_t *dest_of, void *ws, size_t ws_bytes,
+                          moe_stream stream);
+
+/* The inverse gather of moe_ep_regroup: out[i] = o[dest_of[i]] for i < n_recv (expert
+ * outputs, or dXp in the backward, back in the received order for the return exchange).
+ *   o [R_loc x d] bf16 in; dest_of [n_recv] int32 in (from moe_ep_regroup; an entry
+ *   outside [0, R_loc) is skipped); out [n_recv x d] bf16 out. */
+moe_status moe_ep_unregroup(moe_shape s_loc, int64_t n_recv, const moe_bf16 *o,
+                            const int32_t *dest_of, moe_bf16 *out, moe_stream stream);
+
+/* The row gradient of an expert-parallel backward in the compact send order:
+ * gs[row_of[t][j]] = bf16(w[t][j] * dy[t]); with dlogits, also the router-logit
+ * gradient of moe_backward from the returned expert outputs ob (dw_j =
+ * <dy[t], ob[row_of[t][j]]>, dlogits[t][ids[t][j]] = w_j (dw_j - sum_i w_i dw_i), 0
+ * elsewhere). dy [T x d] bf16; w, ids, row_of [T x k]; counts [E], offsets [E+1] from
+ * moe_ep_dispatch; ob [T k x d] bf16 (may be NULL without dlogits); gs [T k x d] bf16
+ * out; dlogits [T x E] fp32 out or NULL. */
+moe_status moe_ep_grad_scatter(moe_shape s, const moe_bf16 *dy, const float *w,
+                               const int32_t *ids, const int32_t *counts, const int32_t *offsets,
+                               const int32_t *row_of, const moe_bf16 *ob, moe_bf16 *gs,
+                               float *dlogits, moe_stream stream);
+
 /* Dispatch without a workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart of this call: it exists for callers that have no
  * way to obtain device memory for a workspace (code running under a runtime that
@@ -280,7 +379,8 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
  *   (T = 65536 with E = 32 and k = 4 fits). Larger shapes return MOE_ERR_WORKSPACE.
  *   The first call on a device looks up the array's device address (set-up, once
  *   per device, with that device current); make that first call before any stream
- *   capture. Every call shares the one array and it keeps the last call's contents:
+ *   capture. The address is kept for the life of the process: do not use this call
+ *   on a device after a cudaDeviceReset of that device. Every call shares the one array and it keeps the last call's contents:
  *   each call writes every entry it reads, so nothing needs clearing, but calls that
  *   overlap on the GPU (other streams or host threads) race and must be ordered by
  *   the caller. */
@@ -300,8 +400,9 @@ moe_status moe_debug_gate_up_withheld(moe_shape s, const moe_bf16 *xp, const int
                                       size_t ws_bytes, int wait_limit_us, moe_stream stream);
 
 /* Device-side status of a workspace or scratch: synchronises `stream`, reads the
- * status word that the kernels set when a pipeline wait runs past its time limit,
- * and clears it. Returns MOE_OK or MOE_ERR_TIMEOUT. */
+ * status word that the kernels set when a pipeline wait runs past its time limit (or,
+ * for moe_ep_regroup, when the received counts are inconsistent), and clears it.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_INVALID_ARG. */
 moe_status moe_check_device_status(const void *ws_or_scratch, moe_stream stream);
 
 /* Launch timing for measurement. While enabled, the library brackets each kernel

@@ -75,6 +75,15 @@ _SIG = {
     "moe_aux_loss_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp]),
     "moe_backward": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_expert_ffn_backward": (ctypes.c_int, [MoEShape] + [_c_vp] * 10 +
+                                [_c_vp, ctypes.c_size_t, _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_ep_local_shape": (ctypes.c_int, [MoEShape, ctypes.c_int, ctypes.POINTER(MoEShape)]),
+    "moe_ep_dispatch": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       ctypes.c_size_t, _c_vp]),
+    "moe_ep_regroup": (ctypes.c_int, [MoEShape, ctypes.c_int, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp,
+                                      _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "moe_ep_unregroup": (ctypes.c_int, [MoEShape, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "moe_ep_grad_scatter": (ctypes.c_int, [MoEShape] + [_c_vp] * 9 + [_c_vp]),
     "moe_check_device_status": (ctypes.c_int, [_c_vp, _c_vp]),
     "moe_debug_gate_up_withheld": (ctypes.c_int, [MoEShape, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                                   ctypes.c_size_t, ctypes.c_int, _c_vp]),
@@ -308,10 +317,12 @@ def expert_ffn(s: MoEShape, xp: torch.Tensor, counts: torch.Tensor, w_gu: torch.
     return h, gu, o
 
 
-def combine(s: MoEShape, o: torch.Tensor, w: torch.Tensor, row_of: torch.Tensor) -> torch.Tensor:
-    """moe_combine: y [T,d] bf16."""
+def combine(s: MoEShape, o: torch.Tensor, w: torch.Tensor | None, row_of: torch.Tensor
+            ) -> torch.Tensor:
+    """moe_combine: y [T,d] bf16 (w None: unit weights, the plain gather-sum)."""
     _want(o, torch.bfloat16, "o")
-    _want(w, torch.float32, "w")
+    if w is not None:
+        _want(w, torch.float32, "w")
     _want(row_of, torch.int32, "row_of")
     y = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=o.device)
     _check(lib().moe_combine(s, _p(o), _p(w), _p(row_of), _p(y), _stream()), "moe_combine")
@@ -423,6 +434,108 @@ def backward(s: MoEShape, dy: torch.Tensor, w_gu: torch.Tensor, w_down: torch.Te
     return dx, dw_gu, dw_down
 
 
+def expert_ffn_backward(s: MoEShape, g: torch.Tensor, xp: torch.Tensor, gu: torch.Tensor,
+                        h: torch.Tensor, counts: torch.Tensor, w_gu: torch.Tensor,
+                        w_down: torch.Tensor, ws: torch.Tensor | None = None,
+                        scratch: torch.Tensor | None = None):
+    """moe_expert_ffn_backward: (dxp [R,d], dw_gu [E,d,2f], dw_down [E,f,d]) for the row
+    gradient g [R,d] (segment-padded, zero padding rows)."""
+    for t, n in ((g, "g"), (xp, "xp"), (gu, "gu"), (h, "h"), (w_gu, "w_gu"), (w_down, "w_down")):
+        _want(t, torch.bfloat16, n)
+    _want(counts, torch.int32, "counts")
+    dev = g.device
+    if ws is None:
+        ws = new_workspace(s, False, dev)
+    if scratch is None:
+        scratch = new_scratch(s, dev)
+    dxp = torch.empty((padded_rows(s), s.d), dtype=torch.bfloat16, device=dev)
+    dw_gu = torch.empty(tuple(w_gu.shape), dtype=torch.bfloat16, device=dev)
+    dw_down = torch.empty(tuple(w_down.shape), dtype=torch.bfloat16, device=dev)
+    _check(lib().moe_expert_ffn_backward(s, _p(g), _p(xp), _p(gu), _p(h), _p(counts), _p(w_gu),
+                                         _p(w_down), _p(dxp), _p(dw_gu), _p(dw_down), _p(ws),
+                                         ws.numel(), _p(scratch), scratch.numel(), _stream()),
+           "moe_expert_ffn_backward")
+    return dxp, dw_gu, dw_down
+
+
+# ----------------------------------------------------------- expert parallelism
+def ep_local_shape(s: MoEShape, G: int) -> MoEShape:
+    """moe_ep_local_shape: the shape of one rank's expert work among G ranks."""
+    out = MoEShape()
+    _check(lib().moe_ep_local_shape(s, int(G), ctypes.byref(out)), "moe_ep_local_shape")
+    return out
+
+
+def ep_dispatch(s: MoEShape, x: torch.Tensor, ids: torch.Tensor,
+                ws: torch.Tensor | None = None) -> dict:
+    """moe_ep_dispatch: the compact send buffer xs [T k, d] sorted by expert, counts [E],
+    offsets [E+1] and row_of [T, k] (compact rows)."""
+    _want(x, torch.bfloat16, "x")
+    _want(ids, torch.int32, "ids")
+    dev = x.device
+    if ws is None:
+        ws = new_workspace(s, False, dev)
+    out = {"xs": torch.empty((s.T * s.k, s.d), dtype=torch.bfloat16, device=dev),
+           "counts": torch.empty((s.E,), dtype=torch.int32, device=dev),
+           "offsets": torch.empty((s.E + 1,), dtype=torch.int32, device=dev),
+           "row_of": torch.empty((s.T, s.k), dtype=torch.int32, device=dev)}
+    _check(lib().moe_ep_dispatch(s, _p(x), _p(ids), _p(out["xs"]), _p(out["counts"]),
+                                 _p(out["offsets"]), _p(out["row_of"]), _p(ws), ws.numel(),
+                                 _stream()), "moe_ep_dispatch")
+    return out
+
+
+def ep_regroup(s_loc: MoEShape, G: int, recv_counts: torch.Tensor, n_recv: int,
+               xr: torch.Tensor, ws: torch.Tensor | None = None) -> dict:
+    """moe_ep_regroup: received rows xr [n_recv, d] (source-major) to the local experts'
+    segment-padded rows xp [R_loc, d]; also counts [El], padded_offsets [El+1], dest_of
+    [n_recv] and the workspace holding the status word."""
+    _want(recv_counts, torch.int32, "recv_counts")
+    _want(xr, torch.bfloat16, "xr")
+    dev = xr.device
+    if ws is None:
+        ws = new_workspace(s_loc, False, dev)
+    out = {"xp": torch.empty((padded_rows(s_loc), s_loc.d), dtype=torch.bfloat16, device=dev),
+           "counts": torch.empty((s_loc.E,), dtype=torch.int32, device=dev),
+           "padded_offsets": torch.empty((s_loc.E + 1,), dtype=torch.int32, device=dev),
+           "dest_of": torch.empty((max(int(n_recv), 1),), dtype=torch.int32, device=dev),
+           "ws": ws}
+    _check(lib().moe_ep_regroup(s_loc, int(G), _p(recv_counts.contiguous()), int(n_recv),
+                                _p(xr) if n_recv else _c_vp(None), _p(out["xp"]),
+                                _p(out["counts"]), _p(out["padded_offsets"]), _p(out["dest_of"]),
+                                _p(ws), ws.numel(), _stream()), "moe_ep_regroup")
+    out["dest_of"] = out["dest_of"][:int(n_recv)]
+    return out
+
+
+def ep_unregroup(s_loc: MoEShape, n_recv: int, o: torch.Tensor, dest_of: torch.Tensor
+                 ) -> torch.Tensor:
+    """moe_ep_unregroup: out [n_recv, d] = o[dest_of]."""
+    _want(o, torch.bfloat16, "o")
+    _want(dest_of, torch.int32, "dest_of")
+    out = torch.empty((int(n_recv), s_loc.d), dtype=torch.bfloat16, device=o.device)
+    if n_recv:
+        _check(lib().moe_ep_unregroup(s_loc, int(n_recv), _p(o), _p(dest_of), _p(out),
+                                      _stream()), "moe_ep_unregroup")
+    return out
+
+
+def ep_grad_scatter(s: MoEShape, dy: torch.Tensor, w: torch.Tensor, ids: torch.Tensor,
+                    disp: dict, ob: torch.Tensor | None = None, router_grad: bool = False):
+    """moe_ep_grad_scatter: gs [T k, d] = w dY in the compact send order; with
+    router_grad also dlogits [T, E] from the returned expert outputs ob."""
+    _want(dy, torch.bfloat16, "dy")
+    dev = dy.device
+    gs = torch.empty((s.T * s.k, s.d), dtype=torch.bfloat16, device=dev)
+    dl = torch.empty((s.T, s.E), dtype=torch.float32, device=dev) if router_grad else None
+    if router_grad and ob is None:
+        raise ValueError("the router-logit gradient needs the returned expert outputs ob")
+    _check(lib().moe_ep_grad_scatter(s, _p(dy), _p(w), _p(ids), _p(disp["counts"]),
+                                     _p(disp["offsets"]), _p(disp["row_of"]), _p(ob), _p(gs),
+                                     _p(dl), _stream()), "moe_ep_grad_scatter")
+    return gs, dl
+
+
 def debug_gate_up_withheld(s: MoEShape, xp: torch.Tensor, counts: torch.Tensor,
                            w_gu: torch.Tensor, ws: torch.Tensor, wait_limit_us: int) -> None:
     """moe_debug_gate_up_withheld: the gate_up GEMM with its first loads withheld."""
@@ -457,4 +570,6 @@ __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_siz
            "backward_scratch_size", "new_workspace", "new_scratch", "workspace_views", "route",
            "router_route", "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward",
            "combine", "forward", "forward_router", "backward", "router_backward", "check_device_status",
+           "expert_ffn_backward", "ep_local_shape", "ep_dispatch", "ep_regroup", "ep_unregroup",
+           "ep_grad_scatter",
            "debug_gate_up_withheld", "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

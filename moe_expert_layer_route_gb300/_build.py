@@ -20,7 +20,7 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libmoe_gb300.so")
 
 SOURCES = ["moe_api.cu", "route_dispatch.cu", "router.cu", "grouped_gemm.cu",
-           "dispatch_noalloc.cu"]
+           "dispatch_noalloc.cu", "ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-cudart", "shared", "-Xcompiler", "-fPIC,-O3", "--expt-relaxed-constexpr",
          "-I", CSRC, "-I", INCLUDE]

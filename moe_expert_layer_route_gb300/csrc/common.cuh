@@ -13,6 +13,7 @@ namespace moe {
 // Device status word values (first int32 of every workspace and scratch).
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;
+constexpr int kDevBadCounts = 2;  // received counts inconsistent with the stated row total
 
 // A pipeline wait that runs longer than this gives up, sets the status word and
 // lets the kernel exit. Legitimate waits in these kernels last microseconds.

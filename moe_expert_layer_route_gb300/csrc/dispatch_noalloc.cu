@@ -31,7 +31,9 @@ std::mutex g_setup_mu;
 int32_t *g_scratch_addr[64] = {};  // device address of g_dispatch_scratch, per device
 
 // Set-up, once per device, with that device current: the host-side name of a
-// __device__ array is only a stand-in, the kernels need its device address.
+// __device__ array is only a stand-in, the kernels need its device address. The
+// address is cached for the life of the process, so the library must not be used on
+// a device across a cudaDeviceReset (the cached address would then be stale).
 moe_status scratch_address(int32_t **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -56,12 +58,9 @@ extern "C" moe_status moe_dispatch_noalloc(moe_shape s, const moe_bf16 *x, const
                                            moe_bf16 *xp, int32_t *counts, int32_t *offsets,
                                            int32_t *padded_offsets, int32_t *row_of,
                                            int32_t *tok_of, moe_stream stream) {
-  // the same shape rules as every other entry point
-  if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.f <= 0 || s.k > s.E)
-    return MOE_ERR_INVALID_ARG;
-  if (s.E > 256 || s.k > 16 || s.d > (1 << 20) || s.f > (1 << 20)) return MOE_ERR_UNSUPPORTED;
-  if (s.d % 8 != 0 || s.f % 8 != 0) return MOE_ERR_ALIGNMENT;
-  if (moe_padded_rows(s) < 0) return MOE_ERR_OVERFLOW;  // T*k or the padded rows beyond int32
+  // the same shape rules and device check as every other entry point
+  const moe_status shape_ok = moe::check_shape(s);
+  if (shape_ok != MOE_OK) return shape_ok;
   const void *always[] = {xp, counts, offsets, padded_offsets, tok_of};
   for (const void *p : always) {
     if (!p) return MOE_ERR_INVALID_ARG;
@@ -82,6 +81,8 @@ extern "C" moe_status moe_dispatch_noalloc(moe_shape s, const moe_bf16 *x, const
   const int64_t tiles_at = hist_at + round64(s.E * C);
   const int64_t need = tiles_at + round64(R / moe::kTileRows);
   if (need > kScratchInts) return MOE_ERR_WORKSPACE;  // beyond the fixed 4 MiB scratch
+  const moe_status dev_ok = moe::check_device();
+  if (dev_ok != MOE_OK) return dev_ok;
 
   int32_t *scratch = nullptr;
   const moe_status st0 = scratch_address(&scratch);

@@ -84,6 +84,8 @@ template <int KIND>
 constexpr int epi_warps() {
   return (KIND == GATE_UP || KIND == DOWN || KIND == DGRAD_X) ? 4 : 8;
 }
+// The DGRAD_H epilogue gives each warp one half of the tile's columns (ch_own >= 0).
+static_assert(epi_warps<DGRAD_H>() == 8, "the DGRAD_H epilogue needs two warps per lane quarter");
 template <int KIND>
 constexpr int threads_of() {
   return 64 + 32 * epi_warps<KIND>();

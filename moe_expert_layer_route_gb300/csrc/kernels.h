@@ -5,9 +5,16 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe_gb300.h"
 #include "common.cuh"
 
 namespace moe {
+
+// Host-side checks shared by the entry points (moe_api.cu): the shape rules of the
+// C ABI header, and that the current device is an sm_103 GPU (MOE_ERR_UNSUPPORTED
+// otherwise).
+moe_status check_shape(const moe_shape &s);
+moe_status check_device();
 
 constexpr int kTileRows = 128;  // rows of one GEMM tile; expert segments are padded to it
 
@@ -107,6 +114,18 @@ cudaError_t gemm_wgrad(const GemmPlan &p, const void *x, const void *y, void *dw
 // elements, zero fill out of bounds, swizzle 128 or 64 (bytes).
 cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                               const uint64_t *strides_bytes, const uint32_t *box, int swizzle);
+
+// ep.cu: the received rows (source-major [s][e][rows], recv_counts [G][El]) to the
+// segment-padded expert-major layout of the local experts (zero padding rows), with
+// dest_of[i] the padded row of received row i; status records kDevBadCounts when the
+// counts do not add up to n_recv or overflow the R padded rows (then nothing is written)
+cudaError_t launch_ep_regroup(const int32_t *recv_counts, const void *xr, void *xp,
+                              int32_t *counts_loc, int32_t *padded_loc, int32_t *dest_of,
+                              int *status, int G, int El, int n_recv, int R, int d,
+                              cudaStream_t st);
+// out[i] = o[dest_of[i]] (rows of d bf16), i < n_recv; dest_of outside [0, R) is skipped
+cudaError_t launch_ep_unregroup(const void *o, const int32_t *dest_of, void *out, int n_recv,
+                                int R, int d, cudaStream_t st);
 
 int num_sms();
 

@@ -80,18 +80,6 @@ BwdLayout bwd_layout(const moe_shape &s) {
   return L;
 }
 
-moe_status check_shape(const moe_shape &s) {
-  if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.f <= 0) return MOE_ERR_INVALID_ARG;
-  if (s.k > s.E) return MOE_ERR_INVALID_ARG;
-  if (s.E > 256 || s.k > 16) return MOE_ERR_UNSUPPORTED;
-  if (s.d % 8 != 0 || s.f % 8 != 0) return MOE_ERR_ALIGNMENT;
-  if (s.d > (1 << 20) || s.f > (1 << 20)) return MOE_ERR_UNSUPPORTED;
-  const int64_t lim = (int64_t)1 << 31;
-  if (s.T >= lim / s.k) return MOE_ERR_OVERFLOW;            // T*k fits int32
-  if (padded_rows(s) >= lim) return MOE_ERR_OVERFLOW;       // padded rows fit int32
-  return MOE_OK;
-}
-
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 template <typename... P>
@@ -135,20 +123,6 @@ SideStream *side_stream() {
   return sd.s ? &sd : nullptr;
 }
 
-moe_status check_device() {
-  static int ok[64] = {};  // 0 unknown, 1 good, -1 unsupported
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  int &v = ok[dev & 63];
-  if (v == 0) {
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    v = (major == 10 && minor == 3) ? 1 : -1;
-  }
-  return v == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
-}
-
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 #define MOE_TRY(expr)                   \
@@ -190,6 +164,37 @@ const char *overlapped_name(const char *name) {
 }
 
 }  // namespace
+
+namespace moe {
+
+// Host-side checks shared by every entry point (declared in kernels.h).
+moe_status check_shape(const moe_shape &s) {
+  if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.f <= 0) return MOE_ERR_INVALID_ARG;
+  if (s.k > s.E) return MOE_ERR_INVALID_ARG;
+  if (s.E > 256 || s.k > 16) return MOE_ERR_UNSUPPORTED;
+  if (s.d % 8 != 0 || s.f % 8 != 0) return MOE_ERR_ALIGNMENT;
+  if (s.d > (1 << 20) || s.f > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  const int64_t lim = (int64_t)1 << 31;
+  if (s.T >= lim / s.k) return MOE_ERR_OVERFLOW;            // T*k fits int32
+  if (padded_rows(s) >= lim) return MOE_ERR_OVERFLOW;       // padded rows fit int32
+  return MOE_OK;
+}
+
+moe_status check_device() {
+  static int ok[64] = {};  // 0 unknown, 1 good, -1 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int &v = ok[dev & 63];
+  if (v == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    v = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return v == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace moe
 
 namespace moe {
 
@@ -328,10 +333,12 @@ moe_status moe_combine(moe_shape s, const moe_bf16 *o, const float *w, const int
                        moe_bf16 *y, moe_stream stream) {
   MOE_TRY(check_shape(s));
   if (s.T == 0) return MOE_OK;
-  MOE_TRY(check_ptrs(o, w, row_of, y));
+  MOE_TRY(check_ptrs(o, row_of, y));
+  if (w && !aligned16(w)) return MOE_ERR_ALIGNMENT;
   MOE_TRY(check_device());
-  MOE_CUDA(launch_combine(o, w, row_of, y, (int)s.T, (int)s.d, (int)s.k,
-                          static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (w) MOE_CUDA(launch_combine(o, w, row_of, y, (int)s.T, (int)s.d, (int)s.k, st));
+  else MOE_CUDA(launch_gather_sum(o, row_of, y, (int)s.T, (int)s.d, (int)s.k, st));
   return MOE_OK;
 }
 
@@ -461,6 +468,118 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   return MOE_OK;
 }
 
+moe_status moe_expert_ffn_backward(moe_shape s, const moe_bf16 *g, const moe_bf16 *xp,
+                                   const moe_bf16 *gu, const moe_bf16 *h, const int32_t *counts,
+                                   const moe_bf16 *w_gu, const moe_bf16 *w_down, moe_bf16 *dxp,
+                                   moe_bf16 *dw_gu, moe_bf16 *dw_down, void *ws, size_t ws_bytes,
+                                   void *scratch, size_t scratch_bytes, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(g, xp, gu, h, counts, w_gu, w_down, dxp, dw_gu, dw_down, ws, scratch));
+  const FwdLayout L = fwd_layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const BwdLayout B = bwd_layout(s);
+  if (scratch_bytes < B.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int E = (int)s.E, d = (int)s.d, f = (int)s.f;
+  int *status = at<int>(ws, L.status);
+  int32_t *padded = at<int32_t>(ws, L.padded), *tiles = at<int32_t>(ws, L.tile_expert);
+  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
+  void *dgu = at<void>(scratch, B.dgu);
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOE_CUDA(launch_plan(counts, E, at<int32_t>(ws, L.offsets), padded, tiles, pstart, pexp, st));
+  const GemmPlan p{padded, counts, tiles, pstart, pexp, E, padded_rows(s), s.T * s.k / s.E};
+  MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));
+  MOE_CUDA(gemm_wgrad(p, h, g, dw_down, f, d, status, "gemm_wgrad_down", st));
+  MOE_CUDA(gemm_dgrad_x(p, dgu, w_gu, dxp, d, f, status, st));
+  MOE_CUDA(gemm_wgrad(p, xp, dgu, dw_gu, d, 2 * f, status, "gemm_wgrad_gu", st));
+  return MOE_OK;
+}
+
+moe_status moe_ep_local_shape(moe_shape s, int G, moe_shape *out) {
+  MOE_TRY(check_shape(s));
+  if (!out || G < 1 || G > s.E || s.E % G != 0) return MOE_ERR_INVALID_ARG;
+  moe_shape l = s;
+  l.E = s.E / G;
+  l.T = s.T * G;
+  l.k = s.k < l.E ? s.k : l.E;
+  MOE_TRY(check_shape(l));
+  *out = l;
+  return MOE_OK;
+}
+
+moe_status moe_ep_dispatch(moe_shape s, const moe_bf16 *x, const int32_t *ids, moe_bf16 *xs,
+                           int32_t *counts, int32_t *offsets, int32_t *row_of, void *ws,
+                           size_t ws_bytes, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_ptrs(counts, offsets, ws));
+  if (s.T > 0) MOE_TRY(check_ptrs(x, ids, xs, row_of));
+  const FwdLayout L = fwd_layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = (int)s.T, E = (int)s.E, k = (int)s.k, d = (int)s.d;
+  int32_t *rank = at<int32_t>(ws, L.rank), *hist = at<int32_t>(ws, L.hist);
+  MOE_CUDA(launch_count(ids, rank, hist, T, E, k, st));
+  MOE_CUDA(launch_scan(hist, T, E, k, counts, offsets, at<int32_t>(ws, L.padded),
+                       at<int32_t>(ws, L.tile_expert), nullptr, nullptr, nullptr, nullptr, st));
+  // the compact layout: the segment starts are the compact offsets (no padding rows),
+  // and the row space ends at A = T k
+  if (T > 0)
+    MOE_CUDA(launch_scatter(x, ids, rank, hist, offsets, counts, row_of, at<int32_t>(ws, L.tok_of),
+                            xs, T, d, E, k, T * k, st));
+  return MOE_OK;
+}
+
+moe_status moe_ep_regroup(moe_shape s_loc, int G, const int32_t *recv_counts, int64_t n_recv,
+                          const moe_bf16 *xr, moe_bf16 *xp, int32_t *counts_loc,
+                          int32_t *padded_loc, int32_t *dest_of, void *ws, size_t ws_bytes,
+                          moe_stream stream) {
+  MOE_TRY(check_shape(s_loc));
+  if (G < 1 || G * s_loc.E > 256 || n_recv < 0) return MOE_ERR_INVALID_ARG;
+  if (n_recv > s_loc.T * s_loc.k) return MOE_ERR_WORKSPACE;  // beyond the local row space
+  MOE_TRY(check_ptrs(recv_counts, xp, counts_loc, padded_loc, ws));
+  if (n_recv > 0) MOE_TRY(check_ptrs(xr, dest_of));
+  const FwdLayout L = fwd_layout(s_loc, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_device());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int *status = at<int>(ws, L.status);
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOE_CUDA(launch_ep_regroup(recv_counts, xr, xp, counts_loc, padded_loc, dest_of, status, G,
+                             (int)s_loc.E, (int)n_recv, (int)padded_rows(s_loc), (int)s_loc.d,
+                             st));
+  return MOE_OK;
+}
+
+moe_status moe_ep_unregroup(moe_shape s_loc, int64_t n_recv, const moe_bf16 *o,
+                            const int32_t *dest_of, moe_bf16 *out, moe_stream stream) {
+  MOE_TRY(check_shape(s_loc));
+  if (n_recv < 0) return MOE_ERR_INVALID_ARG;
+  if (n_recv > s_loc.T * s_loc.k) return MOE_ERR_WORKSPACE;
+  if (n_recv == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(o, dest_of, out));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_ep_unregroup(o, dest_of, out, (int)n_recv, (int)padded_rows(s_loc),
+                               (int)s_loc.d, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_ep_grad_scatter(moe_shape s, const moe_bf16 *dy, const float *w,
+                               const int32_t *ids, const int32_t *counts, const int32_t *offsets,
+                               const int32_t *row_of, const moe_bf16 *ob, moe_bf16 *gs,
+                               float *dlogits, moe_stream stream) {
+  MOE_TRY(check_shape(s));
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs(dy, w, ids, counts, offsets, row_of, gs));
+  if (dlogits) MOE_TRY(check_ptrs(dlogits, ob));
+  MOE_TRY(check_device());
+  // compact rows: the segment starts are the compact offsets, so no padding row exists
+  MOE_CUDA(launch_scale_scatter(dy, w, row_of, offsets, counts, gs, (int)s.T, (int)s.d, (int)s.E,
+                                (int)s.k, ob, ids, dlogits, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 size_t moe_router_backward_scratch_size(moe_shape s) {
   if (check_shape(s) != MOE_OK) return 0;
   const int splits = router_dw_splits((int)s.T, (int)s.d, (int)s.E);
@@ -542,7 +661,7 @@ moe_status moe_check_device_status(const void *ws_or_scratch, moe_stream stream)
   if (v != kDevOk) {
     MOE_CUDA(cudaMemsetAsync(const_cast<void *>(ws_or_scratch), 0, sizeof(int), st));
     MOE_CUDA(cudaStreamSynchronize(st));
-    return MOE_ERR_TIMEOUT;
+    return v == kDevBadCounts ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
   }
   return MOE_OK;
 }

@@ -4,8 +4,9 @@ Such callers (code under a runtime that owns every device allocation, or that mu
 not call cudaMalloc at that point) cannot hand the library a workspace, so this
 entry point keeps its scratch in a fixed 4 MiB array inside the library. This file
 checks, through the C ABI, that two calls in a row give exactly what moe_dispatch
-gives with a caller workspace (integer and copy results, so bit-exact, which is the
-bound the dispatch tests use), and that shapes beyond the fixed scratch are refused.
+gives with a caller workspace, and exactly what the CPU oracle's stable counting
+sort gives (integer and copy results, so bit-exact, which is the bound the dispatch
+tests use), and that shapes beyond the fixed scratch are refused.
 It is collected last so that a failure here comes after every other test has run.
 """
 import ctypes
@@ -13,7 +14,9 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import workloads
+from gpu_cases import check_dispatch_exact
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +43,11 @@ def _same_as_dispatch(moe, T, d, E, k, seed):
     for key in ("counts", "offsets", "padded_offsets", "row_of", "tok_of"):
         assert torch.equal(got[key], want[key]), key
     assert torch.equal(got["xp"][:P], want["xp"][:P])
+    # and against the oracle directly: counts, offsets, permutation and row copies
+    rid, _ = oracle.route(inp.logits.numpy(), k)
+    ref = oracle.dispatch(rid, E)
+    ref["ids"] = rid
+    check_dispatch_exact(got, ref, inp.x, k)
 
 
 def test_two_calls_in_a_row_match_the_workspace_dispatch(moe):
