@@ -86,8 +86,14 @@ def test_workload_full_size(moe, name):
         sel = torch.from_numpy(toks_e)
         xs, dys = inp.x[sel].double().numpy(), inp.dy[sel].double().numpy()
         sub_ids, sub_w = rid[toks_e], rw[toks_e]
-        rows = np.array([0, 1, wl.f // 2, wl.f - 1])
-        cols = np.array([0, wl.f - 1, wl.f, 2 * wl.f - 1])
+        # whole rows of dW_down [f x d] and whole columns of dW_gu [d x 2f]: every
+        # sample spans the last (partial) tile along the other axis (d = 2880 = 11.25
+        # tiles of 256), and the samples include rows and columns in the first and the
+        # last tile along their own axis, plus a few at random
+        rows = np.unique(np.concatenate([[0, 1, wl.f // 2, wl.f - 65, wl.f - 1],
+                                         rng.integers(0, wl.f, size=3)]))
+        cols = np.unique(np.concatenate([[0, wl.f - 1, wl.f, 2 * wl.f - 65, 2 * wl.f - 1],
+                                         rng.integers(0, 2 * wl.f, size=3)]))
         dwd = oracle.dw_down_rows(e, rows, xs, dys, sub_ids, sub_w, WG, WD)
         dwg = oracle.dw_gu_cols(e, cols, xs, dys, sub_ids, sub_w, WG, WD)
         got_d = to_np(dw_down[e][torch.from_numpy(rows).to(dev)])
