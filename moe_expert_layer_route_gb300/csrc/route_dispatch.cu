@@ -335,6 +335,11 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict
 // lane's partial sums, then a fixed-order warp reduction), then
 // dlogits[t][ids[t][j]] = w_j (dw_j - sum_i w_i dw_i) and 0 for the other experts. The
 // whole row of each token is written by its warp.
+//
+// KT bounds k (4, 8 or 16: the per-slot arrays are sized by it) and ROUTER says whether
+// the router-logit gradient is formed, so the plain G scatter carries no register for it
+// (the kernel is latency-bound at a few thousand tokens, where occupancy decides).
+template <bool ROUTER, int KT>
 __global__ void __launch_bounds__(256) scale_scatter_kernel(
     const uint4 *__restrict__ dy, const float *__restrict__ w, const int32_t *__restrict__ row_of,
     const int32_t *__restrict__ padded, const int32_t *__restrict__ counts,
@@ -350,25 +355,24 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
       row = row_of[(int64_t)t * k + lane];
       wt = w[(int64_t)t * k + lane];
     }
-    int rows[kMaxK];
-    float wts[kMaxK], dot[kMaxK];
+    int rows[KT];
+    float wts[KT], dot[ROUTER ? KT : 1];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KT; ++j) {
       rows[j] = __shfl_sync(0xffffffffu, row, j);
       wts[j] = __shfl_sync(0xffffffffu, wt, j);
-      dot[j] = 0.f;
+      if (ROUTER) dot[j] = 0.f;
     }
-    const bool router = dlogits != nullptr;
     const uint4 *src = dy + (int64_t)t * nvec;
     for (int v0 = lane; v0 < nvec; v0 += 32 * kVec) {
       uint4 val[kVec];
 #pragma unroll
       for (int u = 0; u < kVec; ++u)
         if (v0 + 32 * u < nvec) val[u] = __ldg(src + v0 + 32 * u);
-      if (router) {
+      if (ROUTER) {
         // the dot products first: kVec output-row loads in flight per slot
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
+        for (int j = 0; j < KT; ++j) {
           if (j < k) {
             const uint4 *orow = o + (int64_t)rows[j] * nvec;
             uint4 ov[kVec];
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
         }
       }
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < KT; ++j) {
         if (j < k) {
           uint4 *dst = g + (int64_t)rows[j] * nvec;
 #pragma unroll
@@ -405,12 +409,12 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
         }
       }
     }
-    if (router) {
+    if (ROUTER) {
       float s = 0.f;
-      int eid[kMaxK];
+      int eid[KT];
       const int my_id = (lane < k) ? ids[(int64_t)t * k + lane] : -1;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < KT; ++j) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], off);
         eid[j] = __shfl_sync(0xffffffffu, my_id, j);
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
       for (int e = lane; e < E; e += 32) {
         float val = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
+        for (int j = 0; j < KT; ++j)
           if (j < k && eid[j] == e) val = wts[j] * (dot[j] - s);
         out[e] = val;
       }
@@ -605,9 +609,20 @@ cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *
                                  float *dlogits, cudaStream_t st) {
   const int token_blocks = ceil_div(T, 8);
   launch_begin(st);
-  scale_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(
-      (const uint4 *)dy, w, row_of, padded, counts, (uint4 *)g, T, d / 8, E, k, token_blocks,
-      (const uint4 *)o, ids, dlogits);
+#define MOE_SCALE_SCATTER(R, KT)                                                             \
+  scale_scatter_kernel<R, KT><<<token_blocks + E, 256, 0, st>>>(                            \
+      (const uint4 *)dy, w, row_of, padded, counts, (uint4 *)g, T, d / 8, E, k, token_blocks, \
+      (const uint4 *)o, ids, dlogits)
+  if (dlogits) {
+    if (k <= 4) MOE_SCALE_SCATTER(true, 4);
+    else if (k <= 8) MOE_SCALE_SCATTER(true, 8);
+    else MOE_SCALE_SCATTER(true, 16);
+  } else {
+    if (k <= 4) MOE_SCALE_SCATTER(false, 4);
+    else if (k <= 8) MOE_SCALE_SCATTER(false, 8);
+    else MOE_SCALE_SCATTER(false, 16);
+  }
+#undef MOE_SCALE_SCATTER
   return note_launch(dlogits ? "g_scatter_router_grad" : "g_scatter", st);
 }
 
