@@ -363,6 +363,13 @@ def measure(moe, wl: workloads.Workload, args, K: int, W: int, world: int, dev,
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     tokens_all = sum_over_ranks(wl.T, world, dev)
 
+    # ---- end to end with host buffers, right after the device-timed region so that
+    # both see the GPU in the same state (clocks under the power cap drift as it warms)
+    e2e = None
+    if want_e2e:
+        e2e = measure_e2e(wl, inp, run_step, x, logits, dy, w_router is not None, K, world,
+                          dev, tokens_all)
+
     # ---- profiled pass: the same K steps with an event pair around every launch, for
     # the per-kernel times, shares and the dominant kernel's roofline
     moe.profile_start(capacity=K * 24)
@@ -412,11 +419,11 @@ def measure(moe, wl: workloads.Workload, args, K: int, W: int, world: int, dev,
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
+        # {workload description: {kernel: {bytes_per_launch, source_hash, ...}}}
         with open(tpath) as fh:
-            tr = json.load(fh).get(dom)
+            tr = json.load(fh).get(wl.description, {}).get(dom)
         srcs = GEMM_SOURCES if dom.startswith("gemm") else BW_SOURCES
-        if tr and tr.get("source_hash") == source_hash(srcs) and \
-                tr.get("workload") == wl.description:
+        if tr and tr.get("source_hash") == source_hash(srcs):
             traffic = tr.get("bytes_per_launch")
     if dkind == "flop":
         ach = damount / (dmean * 1e-3) / 1e12
@@ -476,10 +483,6 @@ def measure(moe, wl: workloads.Workload, args, K: int, W: int, world: int, dev,
         graph = {"ms_per_step": gms, "value": tokens_all / (gms * 1e-3), "unit": UNIT}
         del cg
 
-    e2e = None
-    if want_e2e:
-        e2e = measure_e2e(wl, inp, run_step, x, logits, dy, w_router is not None, K, world,
-                          dev, tokens_all)
     return {"wl": wl, "ms": ms, "value": tokens_all / (ms * 1e-3),
             "ms_median": statistics.median(step_ms), "stages": stages, "roofline": roof,
             "gemm_tflops": gemm_tflops, "gemm_flop": gemm_flop, "step_roofline": step_roofline,
@@ -557,17 +560,18 @@ def measure_e2e(wl, inp, run_step, x, logits, dy, router_gemm: bool, K: int, wor
     run(3)
     torch.cuda.synchronize()
     barrier(world)
-    t0 = time.perf_counter()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(comp)
-    up.wait_event(ev0)
-    down.wait_event(ev0)
-    run(ke)
-    comp.wait_stream(down)          # the last download is part of the timed region
-    ev1.record(comp)
-    torch.cuda.synchronize()
-    wall = (time.perf_counter() - t0) * 1e3 / ke
+    with ClockSampler(gpu_index_of(dev.index or 0)) as clk:
+        t0 = time.perf_counter()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(comp)
+        up.wait_event(ev0)
+        down.wait_event(ev0)
+        run(ke)
+        comp.wait_stream(down)          # the last download is part of the timed region
+        ev1.record(comp)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) * 1e3 / ke
     e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
     h2d = hx.numel() * 2 + (hl.numel() * 4 if not router_gemm else 0) + \
         (hdy.numel() * 2 if wl.backward else 0)
@@ -589,7 +593,7 @@ def measure_e2e(wl, inp, run_step, x, logits, dy, router_gemm: bool, K: int, wor
     d2h_gbs = rate(lambda: hy[0].copy_(bx0, non_blocking=True), hx.numel() * 2)
     return {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-            "copy_gbs_alone": {"h2d": h2d_gbs, "d2h": d2h_gbs},
+            "copy_gbs_alone": {"h2d": h2d_gbs, "d2h": d2h_gbs}, "clocks": clk.summary(),
             "copies": "uploads and downloads on two copy streams, three device buffer sets: "
                       "both directions overlap each other and the neighbouring steps' kernels"}
 
