@@ -572,7 +572,8 @@ def measure_e2e(wl, inp, run_step, x, logits, dy, router_gemm: bool, K: int, wor
         ev1.record(comp)
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) * 1e3 / ke
-    e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1) / ke, wall), world, dev)
+    ev_ms = ev0.elapsed_time(ev1) / ke
+    e2e_ms = max_over_ranks(max(ev_ms, wall), world, dev)
     h2d = hx.numel() * 2 + (hl.numel() * 4 if not router_gemm else 0) + \
         (hdy.numel() * 2 if wl.backward else 0)
     d2h = hx.numel() * 2 * (2 if wl.backward else 1)
@@ -593,6 +594,7 @@ def measure_e2e(wl, inp, run_step, x, logits, dy, router_gemm: bool, K: int, wor
     d2h_gbs = rate(lambda: hy[0].copy_(bx0, non_blocking=True), hx.numel() * 2)
     return {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "ms_per_step_events": ev_ms, "ms_per_step_wall": wall,
             "copy_gbs_alone": {"h2d": h2d_gbs, "d2h": d2h_gbs}, "clocks": clk.summary(),
             "copies": "uploads and downloads on two copy streams, three device buffer sets: "
                       "both directions overlap each other and the neighbouring steps' kernels"}

@@ -150,17 +150,28 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
   for (int e = warp; e < E; e += 32) {
     int32_t running = 0;
     int32_t *h = hist + (int64_t)e * C;
-    for (int c0 = 0; c0 < C; c0 += 32) {
-      const int c = c0 + lane;
-      const int32_t v = (c < C) ? h[c] : 0;
-      int32_t incl = v;
+    // kScanAhead 32-chunk slices are loaded before the first of them is scanned, so the
+    // loads' latency is paid once per group rather than once per slice
+    constexpr int kScanAhead = 8;
+    for (int g0 = 0; g0 < C; g0 += 32 * kScanAhead) {
+      int32_t v[kScanAhead];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int u = 0; u < kScanAhead; ++u) {
+        const int c = g0 + 32 * u + lane;
+        v[u] = (c < C) ? h[c] : 0;
       }
-      if (c < C) h[c] = running + incl - v;
-      running += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int u = 0; u < kScanAhead; ++u) {
+        const int c = g0 + 32 * u + lane;
+        int32_t incl = v[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (c < C) h[c] = running + incl - v[u];
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) {
       s_cnt[e] = running;
