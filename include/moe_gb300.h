@@ -418,6 +418,25 @@ typedef struct {
 moe_status moe_profile_start(int capacity);
 int moe_profile_stop(moe_launch_time *out, int out_capacity);
 
+/* Stage timing of the grouped GEMMs (a measurement aid with no counterpart on the pages).
+ * Only the diagnostic build of the library (compiled with MOE_STAGE_TIMING,
+ * lib/libmoe_gb300_timing.so, built by `python -m moe_expert_layer_route_gb300.stage_timing`)
+ * has it; in the shipped library both calls return MOE_ERR_UNSUPPORTED (the stamps cost ~2%
+ * of the GEMMs' time even unarmed). Armed for one GEMM kind (0 gate_up, 1 down, 2 dgrad_h, 3 dgrad_x,
+ * 4 the weight gradients; -1 disarms), the next launches of that kind have their CTA 0
+ * stamp the SM clock (clock64) at each pipeline stage and each tile into device arrays that
+ * every GPU loading the library holds (8192 stages, 2048 tiles; later launches overwrite
+ * earlier ones). Arming clears the stamps; calls that overlap on the GPU race on them.
+ * moe_stage_timing_read synchronises the device and copies them out:
+ *   stages [8192 x 4] out: per stage, the producer's free-slot wait ended, its loads
+ *     issued, the MMA issuer's full-stage wait ended, its MMAs and commit issued;
+ *   tiles [2048 x 2] out: per tile of CTA 0, accumulator seen ready by its first epilogue
+ *     warp, accumulator released;
+ * and returns the number of stages stamped, or a negative moe_status. */
+moe_status moe_stage_timing_arm(int kind);
+int moe_stage_timing_read(uint64_t *stages, int stage_capacity, uint64_t *tiles,
+                          int tile_capacity);
+
 /* Number of kernels the library has launched since it was loaded. */
 int64_t moe_launch_count(void);
 

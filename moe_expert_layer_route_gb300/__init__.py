@@ -90,6 +90,8 @@ _SIG = {
     "moe_profile_start": (ctypes.c_int, [ctypes.c_int]),
     "moe_profile_stop": (ctypes.c_int, [ctypes.POINTER(_LaunchTime), ctypes.c_int]),
     "moe_launch_count": (_c_i64, []),
+    "moe_stage_timing_arm": (ctypes.c_int, [ctypes.c_int]),
+    "moe_stage_timing_read": (ctypes.c_int, [_c_vp, ctypes.c_int, _c_vp, ctypes.c_int]),
 }
 
 _lib = None
@@ -562,6 +564,29 @@ def profile_stop(capacity: int = 4096) -> list[tuple[str, float]]:
     return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n, capacity))]
 
 
+STAGE_TIMING_STAGES, STAGE_TIMING_TILES = 8192, 2048
+GEMM_KINDS = {"gate_up": 0, "down": 1, "dgrad_h": 2, "dgrad_x": 3, "wgrad": 4}
+
+
+def stage_timing_arm(kind: str | None) -> None:
+    """moe_stage_timing_arm: stamp CTA 0's pipeline stages of one GEMM kind (None: off)."""
+    _check(lib().moe_stage_timing_arm(-1 if kind is None else GEMM_KINDS[kind]),
+           "moe_stage_timing_arm")
+
+
+def stage_timing_read():
+    """moe_stage_timing_read: (stages [n, 4], tiles [m, 2]) int64 SM-clock stamps."""
+    import numpy as np
+    st = np.zeros((STAGE_TIMING_STAGES, 4), dtype=np.uint64)
+    tl = np.zeros((STAGE_TIMING_TILES, 2), dtype=np.uint64)
+    n = lib().moe_stage_timing_read(_c_vp(st.ctypes.data), STAGE_TIMING_STAGES,
+                                    _c_vp(tl.ctypes.data), STAGE_TIMING_TILES)
+    if n < 0:
+        raise MoEError(n, "moe_stage_timing_read")
+    m = int((tl[:, 1] > 0).sum())
+    return st[:n].astype(np.int64), tl[:m].astype(np.int64)
+
+
 def launch_count() -> int:
     return int(lib().moe_launch_count())
 
@@ -571,5 +596,5 @@ __all__ = ["MoEShape", "MoEError", "lib", "shape", "padded_rows", "workspace_siz
            "router_route", "dispatch", "dispatch_noalloc", "expert_ffn", "aux_loss_backward",
            "combine", "forward", "forward_router", "backward", "router_backward", "check_device_status",
            "expert_ffn_backward", "ep_local_shape", "ep_dispatch", "ep_regroup", "ep_unregroup",
-           "ep_grad_scatter",
+           "ep_grad_scatter", "stage_timing_arm", "stage_timing_read",
            "debug_gate_up_withheld", "profile_start", "profile_stop", "launch_count", "LIB_PATH"]

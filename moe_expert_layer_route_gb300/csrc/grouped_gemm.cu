@@ -479,6 +479,21 @@ __device__ __forceinline__ void prefetch_gu_row(const Args &a, const Tile &t, in
   }
 }
 
+// Stage timing (a measurement aid, only in the diagnostic build compiled with
+// MOE_STAGE_TIMING, where it costs ~2% even unarmed; the shipped build has none of it):
+// CTA 0 of the armed GEMM kind stamps clock64() at each pipeline stage -- when the
+// producer's wait for the free slot ended and when its loads were issued, when the MMA
+// issuer's wait for the full stage ended and when its MMAs and commit were issued -- and,
+// per tile, when its first epilogue warp saw the accumulator and when it released it.
+#ifdef MOE_STAGE_TIMING
+#define MOE_STAMP(...) __VA_ARGS__
+__device__ int g_timing_kind = -1;
+__device__ unsigned long long g_stage_times[kTimingStages][4];
+__device__ unsigned long long g_tile_times[kTimingTiles][2];
+#else
+#define MOE_STAMP(...)
+#endif
+
 // Launched with a cluster of 2 when PAIR (see launch_kind).
 template <int KIND, bool PAIR>
 __global__ void __launch_bounds__(threads_of<KIND>(), 1)
@@ -544,6 +559,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
   const Tail tl = tail_split<KIND, PAIR>(full, units);
   const int total = tl.first + (full - tl.first) * tl.split;
   bool failed = false;
+  MOE_STAMP(const bool timing = blockIdx.x == 0 && g_timing_kind == KIND;)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -559,6 +575,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             ok = false;
             break;
           }
+          MOE_STAMP(const bool stamp = timing && issued < kTimingStages;
+                    if (stamp) g_stage_times[issued][0] = clock64();)
           uint8_t *sA = smem + s * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], (kPair ? 2 : 1) * kStageBytes);
           const uint32_t bar_pair = kPair ? mapa_shared(&full_bar[s], 0) : 0;
@@ -570,6 +588,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
                                       kb * Cfg<PAIR>::kSub + j, rank);
             }
           }
+          MOE_STAMP(if (stamp) g_stage_times[issued][1] = clock64();)
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -603,6 +622,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
       int buf = 0;
       uint32_t aph = 0;
       bool ok = true, any = false;
+      MOE_STAMP(int staged = 0;)  // stages consumed (for the stage timing)
       const uint32_t smem_base = smem_u32(smem);
       for (int tile = unit0; tile < total && ok; tile += units) {
         const Tile t = decode<KIND, PAIR>(a, tl, tile, 0);
@@ -623,6 +643,8 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
               ok = false;
               break;
             }
+            MOE_STAMP(const bool stamp = timing && staged < kTimingStages;
+                      if (stamp) g_stage_times[staged][2] = clock64();)
             tc_fence_after();
             const int nk = (kb == t.kt - 1) ? t.klast : Cfg<PAIR>::kBKS / 16;
 #pragma unroll
@@ -643,6 +665,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
             any = true;
             if (kPair) tc_commit_pair(&empty_bar[s]);
             else tc_commit(&empty_bar[s]);
+            MOE_STAMP(if (stamp) g_stage_times[staged][3] = clock64(); ++staged;)
             if (++s == kStages) {
               s = 0;
               ph ^= 1;
@@ -685,6 +708,9 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
         break;
       }
       tc_fence_after();
+      MOE_STAMP(const int tile_no = (tile - unit0) / units;
+                const bool stamp = timing && warp == 2 && lane == 0 && tile_no < kTimingTiles;
+                if (stamp) g_tile_times[tile_no][0] = clock64();)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
       bool released = false;
       for (int ch = ch_own < 0 ? 0 : ch_own; ch < (ch_own < 0 ? 2 : ch_own + 1); ++ch)
@@ -692,6 +718,7 @@ __global__ void __launch_bounds__(threads_of<KIND>(), 1)
                                        &tmO, &tmO2, &acce_bar[buf],
                                        buf ? acce_pair1 : acce_pair0, kPair);
       if (!released) release_acc(lane, &acce_bar[buf], buf ? acce_pair1 : acce_pair0, kPair);
+      MOE_STAMP(if (stamp) g_tile_times[tile_no][1] = clock64();)
       buf ^= 1;
       if (buf == 0) aph ^= 1;
     }
@@ -835,6 +862,30 @@ Args base_args(const GemmPlan &p, int *status) {
 }
 
 }  // namespace
+
+#ifdef MOE_STAGE_TIMING
+cudaError_t stage_timing_arm(int kind) {
+  void *p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_stage_times);
+  if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(g_stage_times));
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_tile_times);
+  if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(g_tile_times));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_timing_kind, &kind, sizeof(int));
+  return e;
+}
+
+cudaError_t stage_timing_read(unsigned long long *stages, unsigned long long *tiles) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(stages, g_stage_times, sizeof(g_stage_times));
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(tiles, g_tile_times, sizeof(g_tile_times));
+  return e;
+}
+#else
+cudaError_t stage_timing_arm(int) { return cudaErrorNotSupported; }
+cudaError_t stage_timing_read(unsigned long long *, unsigned long long *) {
+  return cudaErrorNotSupported;
+}
+#endif
 
 cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                               const uint64_t *strides_bytes, const uint32_t *box, int swizzle) {

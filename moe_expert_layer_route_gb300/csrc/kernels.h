@@ -127,6 +127,14 @@ cudaError_t launch_ep_regroup(const int32_t *recv_counts, const void *xr, void *
 cudaError_t launch_ep_unregroup(const void *o, const int32_t *dest_of, void *out, int n_recv,
                                 int R, int d, cudaStream_t st);
 
+// Stage timing of the grouped GEMMs (grouped_gemm.cu): arm for one kind (0 gate_up, 1
+// down, 2 dgrad_h, 3 dgrad_x, 4 weight gradients; -1 disarms), clearing the stamps; read
+// kTimingStages x 4 and kTimingTiles x 2 stamps (synchronises the device)
+constexpr int kTimingStages = 8192;
+constexpr int kTimingTiles = 2048;
+cudaError_t stage_timing_arm(int kind);
+cudaError_t stage_timing_read(unsigned long long *stages, unsigned long long *tiles);
+
 int num_sms();
 
 }  // namespace moe

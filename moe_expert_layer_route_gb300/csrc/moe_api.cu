@@ -699,6 +699,30 @@ int moe_profile_stop(moe_launch_time *out, int out_capacity) {
   return n;
 }
 
+moe_status moe_stage_timing_arm(int kind) {
+  if (kind < -1 || kind > 4) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_device());
+  const cudaError_t e = stage_timing_arm(kind);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;  // not the diagnostic build
+  MOE_CUDA(e);
+  return MOE_OK;
+}
+
+int moe_stage_timing_read(uint64_t *stages, int stage_capacity, uint64_t *tiles,
+                          int tile_capacity) {
+  if (!stages || !tiles || stage_capacity < kTimingStages || tile_capacity < kTimingTiles)
+    return MOE_ERR_INVALID_ARG;
+  const moe_status dev = check_device();
+  if (dev != MOE_OK) return dev;
+  const cudaError_t e = stage_timing_read(reinterpret_cast<unsigned long long *>(stages),
+                                          reinterpret_cast<unsigned long long *>(tiles));
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  int n = 0;
+  while (n < kTimingStages && stages[4 * n + 3] != 0) ++n;
+  return n;
+}
+
 int64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
