@@ -238,10 +238,12 @@ def oracle_step(oracle, inp_np: dict, n_tok: int, k: int) -> float:
 
 
 def oracle_inputs(inp: workloads.Inputs, backward: bool, w_router=None) -> dict:
-    return {"x": inp.x.float().numpy(), "logits": inp.logits.numpy(),
-            "w_gu": inp.w_gu.float().numpy(), "w_down": inp.w_down.float().numpy(),
-            "dy": inp.dy.float().numpy() if backward else None,
-            "w_router": None if w_router is None else w_router.float().numpy()}
+    """The workload's inputs as the oracle computes in them (fp64, exact widenings of the
+    bf16 values), converted once here rather than expert by expert inside every call."""
+    return {"x": inp.x.double().numpy(), "logits": inp.logits.numpy(),
+            "w_gu": inp.w_gu.double().numpy(), "w_down": inp.w_down.double().numpy(),
+            "dy": inp.dy.double().numpy() if backward else None,
+            "w_router": None if w_router is None else w_router.double().numpy()}
 
 
 def cpu_threads() -> int:
@@ -703,8 +705,12 @@ def run_reference(args, rank, world) -> dict | None:
     inp = workloads.make_inputs(wl, with_dy=wl.backward)
     inp_np = oracle_inputs(inp, wl.backward,
                            workloads.make_router_weight(wl) if args.router_gemm else None)
-    budget = args.reference_seconds / max(1, args.steps + args.warmup)
-    n = 4
+    # each step a token sample: the oracle's cost per step has a floor that does not
+    # shrink with the sample (every expert it touches writes its whole fp64 dW), so the
+    # sample grows until a step takes about half of max(the run's budget per step, 15 s),
+    # the same scale as the cpu_baseline of our arm's line
+    budget = max(args.reference_seconds / max(1, args.steps + args.warmup), 15.0)
+    n = 16
     t = oracle_step(oracle, inp_np, n, wl.k)
     while t < budget / 2 and n * 2 <= wl.T:
         n *= 2
