@@ -262,6 +262,7 @@ def cpu_baseline(wl, inp, seconds: float, w_router=None) -> dict:
     import oracle
     inp_np = oracle_inputs(inp, wl.backward, w_router)
     n = 16
+    oracle_step(oracle, inp_np, n, wl.k)  # the first call pages in its fp64 buffers
     t = oracle_step(oracle, inp_np, n, wl.k)
     while t < seconds / 4 and n < wl.T:
         n = min(wl.T, n * 4)
@@ -705,12 +706,14 @@ def run_reference(args, rank, world) -> dict | None:
     inp = workloads.make_inputs(wl, with_dy=wl.backward)
     inp_np = oracle_inputs(inp, wl.backward,
                            workloads.make_router_weight(wl) if args.router_gemm else None)
-    # each step a token sample: the oracle's cost per step has a floor that does not
-    # shrink with the sample (every expert it touches writes its whole fp64 dW), so the
-    # sample grows until a step takes about half of max(the run's budget per step, 15 s),
-    # the same scale as the cpu_baseline of our arm's line
-    budget = max(args.reference_seconds / max(1, args.steps + args.warmup), 15.0)
+    # each step a token sample sized so that the whole run (sizing, warm-up and the timed
+    # steps) takes about --reference-seconds; the oracle's cost per step has a floor that
+    # does not shrink with the sample (every expert it touches writes its whole fp64 dW),
+    # so at many steps the sample is small and the tokens/s lower than the cpu_baseline of
+    # our arm's line, which times one larger sample
+    budget = args.reference_seconds / (args.steps + args.warmup + 3)
     n = 16
+    oracle_step(oracle, inp_np, n, wl.k)  # the first call pages in its fp64 buffers
     t = oracle_step(oracle, inp_np, n, wl.k)
     while t < budget / 2 and n * 2 <= wl.T:
         n *= 2
@@ -753,7 +756,7 @@ def main(argv=None) -> int:
     ap.add_argument("--no-workloads", action="store_true",
                     help="measure only the headline workload (no `workloads` record)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--reference-seconds", type=float, default=150.0)
+    ap.add_argument("--reference-seconds", type=float, default=180.0)
     ap.add_argument("--router-grad", action="store_true",
                     help="also compute the router-logit gradient in the backward")
     ap.add_argument("--router-gemm", action="store_true",

@@ -78,8 +78,8 @@ __device__ __forceinline__ int ep_block_of(const int32_t *roff, int n, int32_t i
 }
 
 // Blocks [0, row_blocks): one warp per received row i < n_recv: dest_of[i] = its padded
-// row, xp[dest_of[i]] = xr[i]. Blocks [row_blocks, row_blocks + El): block e zeroes local
-// expert e's padding rows. Block 0 also writes counts_loc and padded_loc. When the
+// row, xp[dest_of[i]] = xr[i]. Blocks [row_blocks, row_blocks + El kPadParts) zero the
+// local experts' padding rows, kPadParts blocks per expert. Block 0 also writes counts_loc and padded_loc. When the
 // received counts do not add up to n_recv, or their segments do not fit the R padded
 // rows, nothing is written and status (if given) records kDevBadCounts.
 __global__ void __launch_bounds__(256) ep_regroup_kernel(
@@ -117,10 +117,9 @@ __global__ void __launch_bounds__(256) ep_regroup_kernel(
         if (v0 + 32 * u < nvec) out[v0 + 32 * u] = val[u];
     }
   } else {
-    const int e = blockIdx.x - row_blocks;
-    const int64_t r0 = tb.pad[e] + tb.cnt[e], r1 = tb.pad[e + 1];
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int64_t q = r0 * nvec + threadIdx.x; q < r1 * nvec; q += blockDim.x) xp[q] = zero;
+    const int e = (blockIdx.x - row_blocks) / kPadParts;
+    zero_pad_part(xp, tb.pad[e] + tb.cnt[e], tb.pad[e + 1], (blockIdx.x - row_blocks) % kPadParts,
+                  nvec);
   }
 }
 
@@ -156,7 +155,7 @@ cudaError_t launch_ep_regroup(const int32_t *recv_counts, const void *xr, void *
                               cudaStream_t st) {
   const int row_blocks = ep_cdiv(n_recv, 8) > 0 ? ep_cdiv(n_recv, 8) : 1;
   launch_begin(st);
-  ep_regroup_kernel<<<row_blocks + El, 256, 0, st>>>(
+  ep_regroup_kernel<<<row_blocks + El * kPadParts, 256, 0, st>>>(
       recv_counts, (const uint4 *)xr, (uint4 *)xp, counts_loc, padded_loc, dest_of, status, G,
       El, n_recv, R, d / 8, row_blocks);
   return note_launch("ep_regroup", st);

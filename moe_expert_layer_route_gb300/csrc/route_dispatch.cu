@@ -218,8 +218,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 // Blocks [0, token_blocks): one warp per token; lane j < k computes the padded row of
 // slot j (segment start + chunk base + local rank), then the warp copies x[t] to each
 // of its k rows in 16-byte vectors (read once, written k times).
-// Blocks [token_blocks, token_blocks + E): block e zeroes expert e's padding rows.
-// The last block marks the rows past the last segment (up to R) with tok_of = -1.
+// Blocks [token_blocks, token_blocks + E kPadParts): expert e's padding rows are zeroed
+// (and marked tok_of = -1) by kPadParts blocks. The last block marks the rows past the
+// last segment (up to R) with tok_of = -1.
 __global__ void __launch_bounds__(256) scatter_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ ids,
     const int32_t *__restrict__ rank, const int32_t *__restrict__ hist,
@@ -257,13 +258,13 @@ __global__ void __launch_bounds__(256) scatter_kernel(
         }
       }
     }
-  } else if ((int)blockIdx.x < token_blocks + E) {
-    const int e = blockIdx.x - token_blocks;
+  } else if ((int)blockIdx.x < token_blocks + E * kPadParts) {
+    const int e = (blockIdx.x - token_blocks) / kPadParts;
+    const int part = (blockIdx.x - token_blocks) % kPadParts;
     const int r0 = padded[e] + counts[e], r1 = padded[e + 1];
-    const int64_t n = (int64_t)(r1 - r0) * nvec;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) xp[(int64_t)r0 * nvec + i] = zero;
-    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) tok_of[r] = -1;
+    zero_pad_part(xp, r0, r1, part, nvec);
+    const int a = (int)pad_part_begin(r0, r1, part), b = (int)pad_part_end(r0, r1, part);
+    for (int r = a + threadIdx.x; r < b; r += blockDim.x) tok_of[r] = -1;
   } else {
     // rows past the last segment belong to no expert
     for (int r = padded[E] + threadIdx.x; r < R; r += blockDim.x) tok_of[r] = -1;
@@ -337,8 +338,8 @@ __global__ void __launch_bounds__(256) gather_sum_kernel(const uint4 *__restrict
 }
 
 // ------------------------------------------------------------------ backward scatter
-// G[row_of[t][j]] = bf16(w[t][j] * dY[t]) (one warp per token); the extra E blocks
-// zero each expert's padding rows of G so the GEMMs read zeros there.
+// G[row_of[t][j]] = bf16(w[t][j] * dY[t]) (one warp per token); the extra E kPadParts
+// blocks zero the experts' padding rows of G so the GEMMs read zeros there.
 //
 // With dlogits, the same pass also forms the router-logit gradient of the token
 // ("The hard problems along the way" in "Halo: Frontier-Lab Training for Everyone":
@@ -441,11 +442,9 @@ __global__ void __launch_bounds__(256) scale_scatter_kernel(
       }
     }
   } else {
-    const int e = blockIdx.x - token_blocks;
-    const int r0 = padded[e] + counts[e], r1 = padded[e + 1];
-    const int64_t n = (int64_t)(r1 - r0) * nvec;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) g[(int64_t)r0 * nvec + i] = zero;
+    const int e = (blockIdx.x - token_blocks) / kPadParts;
+    zero_pad_part(g, padded[e] + counts[e], padded[e + 1], (blockIdx.x - token_blocks) % kPadParts,
+                  nvec);
   }
 }
 
@@ -569,7 +568,7 @@ cudaError_t launch_scatter(const void *x, const int32_t *ids, const int32_t *ran
   const int C = ceil_div(T, kChunk);
   const int token_blocks = ceil_div(T, 8);
   launch_begin(st);
-  scatter_kernel<<<token_blocks + E + 1, 256, 0, st>>>(
+  scatter_kernel<<<token_blocks + E * kPadParts + 1, 256, 0, st>>>(
       (const uint4 *)x, ids, rank, hist, padded, counts, row_of, tok_of, (uint4 *)xp, T, d / 8,
       E, k, C, token_blocks, R);
   return note_launch("scatter", st);
@@ -621,7 +620,7 @@ cudaError_t launch_scale_scatter(const void *dy, const float *w, const int32_t *
   const int token_blocks = ceil_div(T, 8);
   launch_begin(st);
 #define MOE_SCALE_SCATTER(R, KT)                                                             \
-  scale_scatter_kernel<R, KT><<<token_blocks + E, 256, 0, st>>>(                            \
+  scale_scatter_kernel<R, KT><<<token_blocks + E * kPadParts, 256, 0, st>>>(                \
       (const uint4 *)dy, w, row_of, padded, counts, (uint4 *)g, T, d / 8, E, k, token_blocks, \
       (const uint4 *)o, ids, dlogits)
   if (dlogits) {
