@@ -631,6 +631,8 @@ def summary_of(m: dict) -> dict:
             "e2e": None if m["e2e"] is None else m["e2e"]["value"],
             "gemm_tflops": m["gemm_tflops"],
             "gemm_frac_of_bf16_peak": m["gemm_tflops"] / pk["bf16_tflops"],
+            "gemm_frac_of_bf16_sustained": m["gemm_tflops"] / pk["bf16_tflops_sustained"],
+            "gemm_frac_of_nominal_dense": m["gemm_tflops"] / NOMINAL_BF16_TFLOPS,
             "step_roofline_frac": m["step_roofline"]["frac"],
             "step_bound": m["step_roofline"]["bound"],
             "gemms": gemms, "bandwidth_kernels": bw, "experts": m["experts"],
@@ -678,6 +680,7 @@ def run_ours(args, rank, world, local_rank) -> dict | None:
                          f"weights alone are {6 * wl.E * wl.d * wl.f / 1e9:.2f} GB"},
         "gemm_tflops": head["gemm_tflops"],
         "gemm_frac_of_bf16_peak": head["gemm_tflops"] / pk["bf16_tflops"],
+        "gemm_frac_of_bf16_sustained": head["gemm_tflops"] / pk["bf16_tflops_sustained"],
         "gemm_frac_of_nominal_dense": head["gemm_tflops"] / NOMINAL_BF16_TFLOPS,
         "gemm_flop_per_step": head["gemm_flop"],
         "ms_per_step_median": head["ms_median"],
