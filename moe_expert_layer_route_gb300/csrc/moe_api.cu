@@ -460,11 +460,14 @@ moe_status moe_backward(moe_shape s, const moe_bf16 *dy, const moe_bf16 *w_gu,
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOE_CUDA(launch_scale_scatter(dy, w, row_of, padded, counts, g, T, d, E, k, o, ids,
                                 s.T > 0 ? dlogits : nullptr, st));
+  // dX first (the input gradient is what the layer below waits for), its gather right
+  // after dgrad_x so that it reads dXp while the L2 still holds much of it (at
+  // gpt_oss_20b 22 us against 27 us after the weight gradients), then the weight gradients
   MOE_CUDA(gemm_dgrad_h(p, g, w_down, gu, dgu, d, f, status, st));
-  MOE_CUDA(gemm_wgrad(p, h, g, dw_down, f, d, status, "gemm_wgrad_down", st));
   MOE_CUDA(gemm_dgrad_x(p, dgu, w_gu, dxp, d, f, status, st));
-  MOE_CUDA(gemm_wgrad(p, xp, dgu, dw_gu, d, 2 * f, status, "gemm_wgrad_gu", st));
   MOE_CUDA(launch_gather_sum(dxp, row_of, dx, T, d, k, st));
+  MOE_CUDA(gemm_wgrad(p, h, g, dw_down, f, d, status, "gemm_wgrad_down", st));
+  MOE_CUDA(gemm_wgrad(p, xp, dgu, dw_gu, d, 2 * f, status, "gemm_wgrad_gu", st));
   return MOE_OK;
 }
 

@@ -48,9 +48,10 @@ FFN_CASES = [
     (256, 2048, 128, 8, 768, 14, False), # Qwen3-MoE-like widths, many near-empty experts
     (512, 256, 32, 4, 256, 15, True),    # skewed: empty experts, one expert gets every token
     (200, 128, 1, 1, 64, 16, False),     # E = 1: a dense SwiGLU MLP
-    # >= 384 rows per expert: the GEMMs run on SM pairs (256-row pair-tiles; an odd
+    # >= 256 rows per expert: the GEMMs run on SM pairs (256-row pair-tiles; an odd
     # tile count leaves the second half of an expert's last pair-tile unused)
     (1024, 256, 4, 2, 320, 17, False),
+    (640, 256, 5, 2, 320, 22, False),    # 256 rows per expert: the smallest that pairs
     (900, 200, 3, 2, 200, 18, False),
     (300, 64, 256, 16, 64, 19, False),   # the largest E and k: 256 experts of ~19 rows
     (200, 64, 4, 2, 24, 20, False),      # f = 24: gate and up N tiles of 24 columns
@@ -164,6 +165,7 @@ BWD_CASES = [
     (200, 128, 1, 1, 64, 44, False),
     (1, 64, 4, 2, 64, 45, False),
     (1024, 256, 4, 2, 320, 46, False),   # SM-pair GEMMs (see FFN_CASES)
+    (640, 256, 5, 2, 320, 52, False),    # 256 rows per expert, about half in 3 tiles
     (900, 200, 3, 2, 200, 47, False),
     (1024, 384, 4, 2, 576, 48, False),   # pairs with N tails in every GEMM (384, 576, 1152)
     (300, 64, 256, 16, 64, 49, False),   # the largest E and k
