@@ -36,6 +36,14 @@ __device__ __forceinline__ void zero_pad_part(uint4 *__restrict__ base, int64_t 
 }
 
 // ---------------------------------------------------------------------------- route
+// An unsigned key with the order of the fp32 scores: non-negative values above negative
+// ones, magnitudes in the right direction on each side; -0 is taken as +0 so that the two
+// zeros tie, as they compare equal.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t b = (x == 0.f) ? 0u : __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // One warp routes NTOK tokens at once (their shuffle chains interleave, which hides
 // the shuffle latency). Lane l holds logits l, l+32, ..., l+32(Q-1) of each token
 // (E <= 32 Q). k rounds of a warp arg-max of the score under the order (score
@@ -77,45 +85,38 @@ __device__ __forceinline__ void route_tokens(const float *__restrict__ row0, int
     my_l[n] = 0.f;
     my_i[n] = -1;
   }
+  // Each score as an order-preserving unsigned key (equal scores, +0 and -0 included,
+  // give equal keys; every finite score maps above 0, which marks "none"). A round's
+  // arg-max is then two warp reductions: the largest key, and the lowest expert index
+  // among the lanes whose own best candidate has it.
+  uint32_t key[NTOK][Q];
+#pragma unroll
+  for (int n = 0; n < NTOK; ++n)
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+      key[n][q] = ((taken[n] >> q) & 1u) ? 0u : order_key(sc[n][q]);
   for (int j = 0; j < k; ++j) {
-    float bv[NTOK];
+    uint32_t best[NTOK];
     int bi[NTOK];
 #pragma unroll
     for (int n = 0; n < NTOK; ++n) {
-      bv[n] = 0.f;
+      best[n] = 0u;
       bi[n] = 0x7fffffff;  // "none"
 #pragma unroll
       for (int q = 0; q < Q; ++q) {
-        if (!((taken[n] >> q) & 1u)) {
-          // candidates in ascending index: strict '>' keeps the lower index on ties
-          if (bi[n] == 0x7fffffff || sc[n][q] > bv[n]) {
-            bv[n] = sc[n][q];
-            bi[n] = lane + 32 * q;
-          }
+        // candidates in ascending index: strict '>' keeps the lower index on ties
+        if (!((taken[n] >> q) & 1u) && key[n][q] > best[n]) {
+          best[n] = key[n][q];
+          bi[n] = lane + 32 * q;
         }
       }
     }
-    // each butterfly step issues the shuffles of all NTOK tokens before using any
+    uint32_t top[NTOK];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov[NTOK];
-      int oi[NTOK];
+    for (int n = 0; n < NTOK; ++n) top[n] = __reduce_max_sync(0xffffffffu, best[n]);
 #pragma unroll
-      for (int n = 0; n < NTOK; ++n) {
-        ov[n] = __shfl_xor_sync(0xffffffffu, bv[n], off);
-        oi[n] = __shfl_xor_sync(0xffffffffu, bi[n], off);
-      }
-#pragma unroll
-      for (int n = 0; n < NTOK; ++n) {
-        const bool better = (oi[n] != 0x7fffffff) &&
-                            (bi[n] == 0x7fffffff || ov[n] > bv[n] ||
-                             (ov[n] == bv[n] && oi[n] < bi[n]));
-        if (better) {
-          bv[n] = ov[n];
-          bi[n] = oi[n];
-        }
-      }
-    }
+    for (int n = 0; n < NTOK; ++n)
+      bi[n] = __reduce_min_sync(0xffffffffu, best[n] == top[n] ? bi[n] : 0x7fffffff);
     float lv[NTOK];
 #pragma unroll
     for (int n = 0; n < NTOK; ++n) {

@@ -102,22 +102,55 @@ __device__ void plan_from_counts(const int32_t *s_cnt, int E, int32_t *__restric
                                  int32_t *__restrict__ pair_start,
                                  int32_t *__restrict__ pair_expert, int32_t *s_pad,
                                  int32_t *s_pair) {
-  if (threadIdx.x == 0) {
-    int32_t off = 0, pad = 0, pairs = 0;
-    for (int e = 0; e < E; ++e) {
-      offsets[e] = off;
-      padded[e] = pad;
-      s_pad[e] = pad;
-      s_pair[e] = pairs;
-      const int tiles = (s_cnt[e] + kTileRows - 1) / kTileRows;
-      off += s_cnt[e];
-      pad += tiles * kTileRows;
-      pairs += (tiles + 1) / 2;
+  if (threadIdx.x < 32) {
+    // warp 0: lane l takes experts [l kPer, (l+1) kPer); exclusive prefixes over the
+    // lanes by shuffles, then each lane walks its experts in order
+    constexpr int kPer = kMaxE / 32;
+    const int lane = threadIdx.x;
+    int32_t n_rows = 0, n_tiles = 0, n_pairs = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      if (e < E) {
+        const int tiles = (s_cnt[e] + kTileRows - 1) / kTileRows;
+        n_rows += s_cnt[e];
+        n_tiles += tiles;
+        n_pairs += (tiles + 1) / 2;
+      }
     }
-    offsets[E] = off;
-    padded[E] = pad;
-    s_pad[E] = pad;
-    s_pair[E] = pairs;
+    int32_t rows = n_rows, tiles_in = n_tiles, pairs_in = n_pairs;  // inclusive over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t a = __shfl_up_sync(0xffffffffu, rows, o);
+      const int32_t b = __shfl_up_sync(0xffffffffu, tiles_in, o);
+      const int32_t c = __shfl_up_sync(0xffffffffu, pairs_in, o);
+      if (lane >= o) {
+        rows += a;
+        tiles_in += b;
+        pairs_in += c;
+      }
+    }
+    int32_t off = rows - n_rows, til = tiles_in - n_tiles, pairs = pairs_in - n_pairs;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      if (e < E) {
+        offsets[e] = off;
+        padded[e] = til * kTileRows;
+        s_pad[e] = til * kTileRows;
+        s_pair[e] = pairs;
+        const int tiles = (s_cnt[e] + kTileRows - 1) / kTileRows;
+        off += s_cnt[e];
+        til += tiles;
+        pairs += (tiles + 1) / 2;
+      }
+    }
+    if (lane == 31) {
+      offsets[E] = rows;
+      padded[E] = tiles_in * kTileRows;
+      s_pad[E] = tiles_in * kTileRows;
+      s_pair[E] = pairs_in;
+    }
   }
   __syncthreads();
   const int ntiles = s_pad[E] / kTileRows;
@@ -147,37 +180,55 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
   __shared__ int32_t s_pad[kMaxE + 1];
   __shared__ int32_t s_pair[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 32) {
-    int32_t running = 0;
+  // The warp's work items are (expert, group of kScanAhead 32-chunk slices) in order:
+  // experts warp, warp + 32, ..., each group by group. The next item's slices are loaded
+  // before the current one is scanned, so a load's latency overlaps the previous scan.
+  constexpr int kScanAhead = 8;
+  // (one empty group when C = 0, so that every expert's count is still written)
+  const int ngroups = max(1, (C + 32 * kScanAhead - 1) / (32 * kScanAhead));
+  const int items = (warp < E ? (E - warp + 31) / 32 : 0) * ngroups;
+  int32_t v[kScanAhead], vn[kScanAhead];
+  auto load = [&](int it, int32_t(&dst)[kScanAhead]) {
+    const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * 32 * kScanAhead;
+    const int32_t *h = hist + (int64_t)e * C;
+#pragma unroll
+    for (int u = 0; u < kScanAhead; ++u) {
+      const int c = g0 + 32 * u + lane;
+      dst[u] = (c < C) ? h[c] : 0;
+    }
+  };
+  if (items > 0) load(0, v);
+  int32_t running = 0;
+  for (int it = 0; it < items; ++it) {
+    if (it + 1 < items) load(it + 1, vn);
+    const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * 32 * kScanAhead;
     int32_t *h = hist + (int64_t)e * C;
-    // kScanAhead 32-chunk slices are loaded before the first of them is scanned, so the
-    // loads' latency is paid once per group rather than once per slice
-    constexpr int kScanAhead = 8;
-    for (int g0 = 0; g0 < C; g0 += 32 * kScanAhead) {
-      int32_t v[kScanAhead];
+    // all kScanAhead slices, those past C on zeros: their shuffle chains are independent
+    // and interleave (skipping the empty ones serialised the rest: slower at C = 2048)
 #pragma unroll
-      for (int u = 0; u < kScanAhead; ++u) {
-        const int c = g0 + 32 * u + lane;
-        v[u] = (c < C) ? h[c] : 0;
+    for (int u = 0; u < kScanAhead; ++u) {
+      const int c = g0 + 32 * u + lane;
+      int32_t incl = v[u];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
       }
-#pragma unroll
-      for (int u = 0; u < kScanAhead; ++u) {
-        const int c = g0 + 32 * u + lane;
-        int32_t incl = v[u];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += o;
-        }
-        if (c < C) h[c] = running + incl - v[u];
-        running += __shfl_sync(0xffffffffu, incl, 31);
+      if (c < C) h[c] = running + incl - v[u];
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (g0 + 32 * kScanAhead >= C) {  // the expert's last group
+      if (lane == 0) {
+        s_cnt[e] = running;
+        counts[e] = running;
       }
+      running = 0;
     }
-    if (lane == 0) {
-      s_cnt[e] = running;
-      counts[e] = running;
-    }
-    if (prob_part) {
+#pragma unroll
+    for (int u = 0; u < kScanAhead; ++u) v[u] = vn[u];
+  }
+  if (prob_part) {
+    for (int e = warp; e < E; e += 32) {
       float acc = 0.f;  // lane-strided chunks, then a fixed butterfly: a fixed order
       for (int c = lane; c < C; c += 32) acc += prob_part[(int64_t)e * C + c];
 #pragma unroll

@@ -78,12 +78,17 @@ def test_route_bit_exact(moe, c):
     np.testing.assert_allclose(to_np(w), rw, rtol=W_REL, atol=0)
 
 
-def test_route_ties_take_the_lower_index(moe):
-    rng = np.random.default_rng(21)
-    logits = (rng.integers(-2, 3, size=(999, 40)).astype(np.float32) * np.float32(0.25))
+@pytest.mark.parametrize("E", [40, 200])
+def test_route_ties_take_the_lower_index(moe, E):
+    rng = np.random.default_rng(21 + E)
+    logits = (rng.integers(-2, 3, size=(999, E)).astype(np.float32) * np.float32(0.25))
     logits[:5] = 0.0
     logits[5, :] = -0.0
     logits[5, 7] = 0.0
+    # +0 and -0 mixed among negative scores: the two zeros are equal scores
+    zeros = rng.random((999, E)) < 0.3
+    signs = np.where(rng.random((999, E)) < 0.5, np.float32(-0.0), np.float32(0.0))
+    logits[6:] = np.where(zeros[6:], signs[6:], -np.abs(logits[6:]) - np.float32(0.25))
     for k in (1, 3, 8, 16):
         ids, w = moe.route(torch.from_numpy(logits).to(DEV), k)
         rid, rw = oracle.route(logits, k)
