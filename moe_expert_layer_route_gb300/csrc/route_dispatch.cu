@@ -203,19 +203,24 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
     if (it + 1 < items) load(it + 1, vn);
     const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * 32 * kScanAhead;
     int32_t *h = hist + (int64_t)e * C;
-    // all kScanAhead slices, those past C on zeros: their shuffle chains are independent
-    // and interleave (skipping the empty ones serialised the rest: slower at C = 2048)
+    // the slices in two halves, the second skipped when it holds no chunk (C <= 128 at
+    // the group's start); within a half the shuffle chains are independent and interleave
+    // (skipping single slices serialised them: slower at C = 2048)
 #pragma unroll
-    for (int u = 0; u < kScanAhead; ++u) {
-      const int c = g0 + 32 * u + lane;
-      int32_t incl = v[u];
+    for (int half = 0; half < 2; ++half) {
+      if (half == 1 && g0 + 32 * (kScanAhead / 2) >= C) break;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int u = half * (kScanAhead / 2); u < (half + 1) * (kScanAhead / 2); ++u) {
+        const int c = g0 + 32 * u + lane;
+        int32_t incl = v[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (c < C) h[c] = running + incl - v[u];
+        running += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (c < C) h[c] = running + incl - v[u];
-      running += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (g0 + 32 * kScanAhead >= C) {  // the expert's last group
       if (lane == 0) {
