@@ -37,7 +37,9 @@ def _load():
     return moe
 
 
-def _summary(st: np.ndarray, tl: np.ndarray) -> dict:
+def _summary(st: np.ndarray, tl: np.ndarray, kt: int | None = None) -> dict:
+    """kt: stages per tile when every tile of the kind has the same K (the ragged-M
+    kinds), to split the spacing into the first stage of a tile and the others."""
     t0 = st[0, 0]
     pe, pi, mf, mi = (st[:, j] - t0 for j in range(4))
     out = {"stages": int(len(st)), "cycles": int(mi[-1]),
@@ -46,6 +48,19 @@ def _summary(st: np.ndarray, tl: np.ndarray) -> dict:
            "waited_for_data_median": float(np.median(mf[1:] - mi[:-1])),
            "tma_issue_to_data_median": float(np.median(mf - pi)),
            "tiles": int(len(tl))}
+    if kt and len(mi) > kt:
+        first = (np.arange(1, len(mi)) % kt) == 0  # spacing that ends at a tile's first stage
+        sp, wait, lat = np.diff(mi), mf[1:] - mi[:-1], (mf - pi)[1:]
+        out.update({
+            "stages_per_tile": int(kt),
+            "tile_first_stage_spacing_mean": float(sp[first].mean()),
+            "other_stage_spacing_mean": float(sp[~first].mean()),
+            "tile_first_stage_wait_mean": float(wait[first].mean()),
+            "tile_first_stage_tma_latency_mean": float(lat[first].mean()),
+            "other_stage_tma_latency_mean": float(lat[~first].mean()),
+            # the producer's wait for a free slot before each of those stages
+            "tile_first_stage_producer_slot_wait_mean": float((pi - pe)[1:][first].mean()),
+        })
     if len(tl):
         out["epilogue_per_tile_median"] = float(np.median(tl[:, 1] - tl[:, 0]))
     if len(tl) > 1:
@@ -70,6 +85,11 @@ def run(workload: str = "gpt_oss_20b") -> dict:
 
     step()
     torch.cuda.synchronize()
+    # stages per tile of the ragged-M kinds: K / (K per stage), 128 on SM pairs, 64 on
+    # single CTAs (pairs from 256 rows per expert)
+    bks = 128 if wl.T * wl.k // wl.E >= 256 else 64
+    kts = {"gate_up": -(-wl.d // bks), "down": -(-wl.f // bks), "dgrad_h": -(-wl.d // bks),
+           "dgrad_x": -(-2 * wl.f // bks)}
     res = {}
     try:
         for kind in ("gate_up", "down", "dgrad_h", "dgrad_x", "wgrad"):
@@ -77,7 +97,7 @@ def run(workload: str = "gpt_oss_20b") -> dict:
             step()
             st, tl = moe.stage_timing_read()
             if len(st) > 1:
-                res[kind] = _summary(st, tl)
+                res[kind] = _summary(st, tl, kts.get(kind))
     finally:
         moe.stage_timing_arm(None)
     return res
