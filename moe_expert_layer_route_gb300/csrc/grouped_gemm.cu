@@ -104,7 +104,7 @@ struct Args {
   int m_tiles;  // WGRAD: (pair-)tiles along M of one expert's dW
   int k_tiles;  // ragged-M kinds: K / (K per stage), rounded up
   int k_last;   // ragged-M kinds: 16-wide K slices of the last stage that hold columns
-  int weight_stationary;  // ragged-M tile order
+  int weight_stationary;  // short experts: ragged-M and weight-gradient tile orders
   int M_out;    // WGRAD: rows of dW[e]
   int N_out;    // valid output columns
   int f;        // SwiGLU width (GATE_UP, DGRAD_H)
@@ -177,11 +177,21 @@ __device__ __forceinline__ Tile decode_tile(const Args &a, int tile, int rank) {
   t.n = BN;
   t.klast = Cfg<PAIR>::kBKS / 16;
   if (KIND == WGRAD) {
+    // Long experts (more rows than kWeightStationaryMaxRows): (expert, n-tile, m-tile)
+    // with the m-tile fastest, so a round of the persistent CTAs covers every m-tile of a
+    // few n-tiles and each n panel of the expert (dGU for dW_gu, G for dW_down: K rows x
+    // N columns) is fetched from DRAM fewer times, the m panels being re-read from round
+    // to round. Measured on GB300 at 8192 rows per expert: dW_gu 1.6-3.5% faster, its DRAM
+    // reads 19.9 -> 17.6 GB on one GPU. Short experts keep the n-tile fastest (at 512 rows
+    // the m-fastest order was 3% slower).
     const int per = a.m_tiles * a.n_tiles;
     t.e = tile / per;
     const int r = tile - t.e * per;
-    t.m0 = (r / a.n_tiles) * kMTile + rank * BM;
-    t.n0 = (r % a.n_tiles) * BN;
+    const bool m_fast = !a.weight_stationary;
+    const int fast = m_fast ? a.m_tiles : a.n_tiles;  // one division either way
+    const int slow_i = r / fast, fast_i = r - slow_i * fast;
+    t.m0 = (m_fast ? fast_i : slow_i) * kMTile + rank * BM;
+    t.n0 = (m_fast ? slow_i : fast_i) * BN;
     t.kr0 = a.padded[t.e];
     constexpr int kBKS = Cfg<PAIR>::kBKS;
     t.kt = (a.counts[t.e] + kBKS - 1) / kBKS;  // stages holding the expert's rows
