@@ -5,7 +5,6 @@ the tokens the sum, and only rank 0 prints (and, for the reference arm, works)."
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
