@@ -180,49 +180,46 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
   __shared__ int32_t s_pad[kMaxE + 1];
   __shared__ int32_t s_pair[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The warp's work items are (expert, group of kScanAhead 32-chunk slices) in order:
-  // experts warp, warp + 32, ..., each group by group. The next item's slices are loaded
-  // before the current one is scanned, so a load's latency overlaps the previous scan.
-  constexpr int kScanAhead = 8;
+  // The warp's work items are (expert, group of 128 chunks) in order: experts warp,
+  // warp + 32, ..., each group by group. Lane l takes the group's chunks 4l .. 4l+3: a
+  // running sum over its four, one warp scan of the lane totals, then the four exclusive
+  // prefixes (one 5-step shuffle scan per 128 chunks; a scan per 32-chunk slice took ~4x
+  // the instructions). The next item's chunks are loaded before the current one is
+  // scanned, so a load's latency overlaps the previous scan.
+  constexpr int kPer = 4, kGroup = 32 * kPer;
   // (one empty group when C = 0, so that every expert's count is still written)
-  const int ngroups = max(1, (C + 32 * kScanAhead - 1) / (32 * kScanAhead));
+  const int ngroups = max(1, (C + kGroup - 1) / kGroup);
   const int items = (warp < E ? (E - warp + 31) / 32 : 0) * ngroups;
-  int32_t v[kScanAhead], vn[kScanAhead];
-  auto load = [&](int it, int32_t(&dst)[kScanAhead]) {
-    const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * 32 * kScanAhead;
+  int32_t v[kPer], vn[kPer];
+  auto load = [&](int it, int32_t(&dst)[kPer]) {
+    const int e = warp + 32 * (it / ngroups), c0 = (it % ngroups) * kGroup + kPer * lane;
     const int32_t *h = hist + (int64_t)e * C;
 #pragma unroll
-    for (int u = 0; u < kScanAhead; ++u) {
-      const int c = g0 + 32 * u + lane;
-      dst[u] = (c < C) ? h[c] : 0;
-    }
+    for (int u = 0; u < kPer; ++u) dst[u] = (c0 + u < C) ? h[c0 + u] : 0;
   };
   if (items > 0) load(0, v);
   int32_t running = 0;
   for (int it = 0; it < items; ++it) {
     if (it + 1 < items) load(it + 1, vn);
-    const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * 32 * kScanAhead;
+    const int e = warp + 32 * (it / ngroups), g0 = (it % ngroups) * kGroup;
+    const int c0 = g0 + kPer * lane;
     int32_t *h = hist + (int64_t)e * C;
-    // the slices in two halves, the second skipped when it holds no chunk (C <= 128 at
-    // the group's start); within a half the shuffle chains are independent and interleave
-    // (skipping single slices serialised them: slower at C = 2048)
+    int32_t p[kPer];  // inclusive sums within the lane's four chunks
+    p[0] = v[0];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      if (half == 1 && g0 + 32 * (kScanAhead / 2) >= C) break;
+    for (int u = 1; u < kPer; ++u) p[u] = p[u - 1] + v[u];
+    int32_t incl = p[kPer - 1];
 #pragma unroll
-      for (int u = half * (kScanAhead / 2); u < (half + 1) * (kScanAhead / 2); ++u) {
-        const int c = g0 + 32 * u + lane;
-        int32_t incl = v[u];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += o;
-        }
-        if (c < C) h[c] = running + incl - v[u];
-        running += __shfl_sync(0xffffffffu, incl, 31);
-      }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
-    if (g0 + 32 * kScanAhead >= C) {  // the expert's last group
+    const int32_t base = running + incl - p[kPer - 1];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (c0 + u < C) h[c0 + u] = base + p[u] - v[u];
+    running += __shfl_sync(0xffffffffu, incl, 31);
+    if (g0 + kGroup >= C) {  // the expert's last group
       if (lane == 0) {
         s_cnt[e] = running;
         counts[e] = running;
@@ -230,7 +227,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
       running = 0;
     }
 #pragma unroll
-    for (int u = 0; u < kScanAhead; ++u) v[u] = vn[u];
+    for (int u = 0; u < kPer; ++u) v[u] = vn[u];
   }
   if (prob_part) {
     for (int e = warp; e < E; e += 32) {
