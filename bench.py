@@ -155,6 +155,8 @@ def kernel_work(wl: workloads.Workload) -> dict:
         # bandwidth kernels: bytes the stage must move at least once
         "route_count": ("byte", T * E * 4 + A * 12 + E * C * 4),
         "scan": ("byte", 2 * E * C * 4),
+        # the forward's route + count with the scan run by the last block
+        "route_count_scan": ("byte", T * E * 4 + A * 12 + 3 * E * C * 4),
         "scatter": ("byte", T * d * 2 + A * d * 2 + A * 16),
         "combine": ("byte", A * d * 2 + A * 8 + T * d * 2),
         "g_scatter": ("byte", T * d * 2 + A * d * 2 + A * 8),

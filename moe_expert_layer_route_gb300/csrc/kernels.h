@@ -27,6 +27,17 @@ cudaError_t note_launch(const char *name, cudaStream_t st);
 // route_dispatch.cu
 // bias [E] (selection bias) and prob_part [E x ceil(T/32)] (per-chunk softmax sums for
 // the load-balancing statistics) may be null
+// Outputs of the scan that the fused route + count + scan launch writes; done is a
+// zeroed int32 the launch's blocks take tickets from (left zeroed again).
+struct ScanOut {
+  int32_t *counts = nullptr, *offsets = nullptr, *padded = nullptr, *tile_expert = nullptr,
+          *pair_start = nullptr, *pair_expert = nullptr;
+  float *aux = nullptr;
+  int *done = nullptr;
+};
+cudaError_t launch_route_count_scan(const float *logits, const float *bias, int32_t *ids,
+                                   float *w, int32_t *rank, int32_t *hist, float *prob_part,
+                                   int T, int E, int k, const ScanOut &so, cudaStream_t st);
 cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, float *w,
                          int32_t *rank, int32_t *hist, float *prob_part, int T, int E, int k,
                          bool with_count, cudaStream_t st);

@@ -375,16 +375,28 @@ moe_status forward_impl(moe_shape s, const moe_bf16 *x, const float *logits_in,
   float *w = at<float>(ws, L.w);
   void *xp = at<void>(ws, L.xp), *h = at<void>(ws, L.h), *o = at<void>(ws, L.o);
   void *gu = training ? at<void>(ws, L.gu) : nullptr;
-  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  // the status word and, after it, the ticket counter of the fused route + scan launch
+  MOE_CUDA(cudaMemsetAsync(status, 0, 2 * sizeof(int), st));
   float *prob_part = aux ? at<float>(ws, L.prob_part) : nullptr;
-  if (w_router)
+  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
+  if (w_router) {
     MOE_CUDA(launch_router_route(x, w_router, bias, logits_out, ids, w, rank, hist, prob_part,
                                  status, T, d, E, k, true, st));
-  else
-    MOE_CUDA(launch_route(logits_in, bias, ids, w, rank, hist, prob_part, T, E, k, true, st));
-  int32_t *pstart = at<int32_t>(ws, L.pair_start), *pexp = at<int32_t>(ws, L.pair_expert);
-  MOE_CUDA(launch_scan(hist, T, E, k, counts, at<int32_t>(ws, L.offsets), padded, tiles, pstart,
-                       pexp, prob_part, aux, st));
+    MOE_CUDA(launch_scan(hist, T, E, k, counts, at<int32_t>(ws, L.offsets), padded, tiles,
+                         pstart, pexp, prob_part, aux, st));
+  } else {
+    ScanOut so;
+    so.counts = counts;
+    so.offsets = at<int32_t>(ws, L.offsets);
+    so.padded = padded;
+    so.tile_expert = tiles;
+    so.pair_start = pstart;
+    so.pair_expert = pexp;
+    so.aux = aux;
+    so.done = status + 1;
+    MOE_CUDA(launch_route_count_scan(logits_in, bias, ids, w, rank, hist, prob_part, T, E, k, so,
+                                     st));
+  }
   if (aux && T == 0) MOE_CUDA(cudaMemsetAsync(aux, 0, (2 * E + 1) * sizeof(float), st));
   MOE_CUDA(launch_scatter(x, ids, rank, hist, padded, counts, row_of, tok_of, xp, T, d, E, k,
                           (int)padded_rows(s), st));

@@ -14,11 +14,21 @@ namespace moe {
 
 constexpr int kVec = 4;           // 16-byte vectors each lane keeps in flight in the row copies
 
+__device__ void scan_block(int32_t *__restrict__ hist, int C, int E, int32_t *__restrict__ counts,
+                           int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+                           int32_t *__restrict__ tile_expert, int32_t *__restrict__ pair_start,
+                           int32_t *__restrict__ pair_expert, const float *__restrict__ prob_part,
+                           float *__restrict__ aux, int T, int k);
+
 // Block c routes tokens [32c, 32c+32), one warp per token, and, when COUNT, also
 // writes the chunk histogram and local ranks for the dispatch. With prob_part it also
 // writes prob_part[e][c], the sum over the chunk's tokens (in token order) of the
 // softmax of all E logits, for the load-balancing statistics.
-template <bool COUNT, int Q>
+// With SCAN (and COUNT), the block that finishes last also runs the scan of the chunk
+// counts (scan_block): each block publishes its counts with a fence before taking a
+// ticket from *done, so the block with the last ticket sees every block's counts; it
+// resets *done for the next launch. No block waits for another.
+template <bool COUNT, int Q, bool SCAN>
 __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ logits,
                                                      const float *__restrict__ bias,
                                                      int32_t *__restrict__ ids,
@@ -26,7 +36,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ l
                                                      int32_t *__restrict__ rank,
                                                      int32_t *__restrict__ hist,
                                                      float *__restrict__ prob_part, int T, int E,
-                                                     int k, int C) {
+                                                     int k, int C, ScanOut so) {
   __shared__ int32_t s_ids[kChunk][kMaxK];
   __shared__ float s_prob[kChunk][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -62,6 +72,22 @@ __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ l
     }
   }
   if constexpr (COUNT) count_chunk(s_ids, c, T, E, k, C, warp, 32, lane, rank, hist);
+  if constexpr (COUNT && SCAN) {
+    __shared__ int s_last;
+    __threadfence();  // this thread's hist and prob_part stores, device-wide
+    __syncthreads();  // every thread of the block has stored
+    if (threadIdx.x == 0) {
+      __threadfence();  // cumulative: the block's stores before its ticket
+      s_last = atomicAdd(so.done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();  // the other blocks' stores before this block's reads
+      scan_block(hist, C, E, so.counts, so.offsets, so.padded, so.tile_expert, so.pair_start,
+                 so.pair_expert, prob_part, so.aux, T, k);
+      if (threadIdx.x == 0) *so.done = 0;
+    }
+  }
 }
 
 // Histogram and local ranks from ids already in memory (standalone dispatch).
@@ -166,15 +192,14 @@ __device__ void plan_from_counts(const int32_t *s_cnt, int E, int32_t *__restric
 // With prob_part, also the load-balancing statistics: aux[e] = f_e = counts_e / (T k),
 // aux[E + e] = P_e = (sum over chunks, in chunk order, of prob_part[e][c]) / T and
 // aux[2E] = E * sum_e f_e P_e (summed in expert order).
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, int C, int E,
-                                                    int32_t *__restrict__ counts,
-                                                    int32_t *__restrict__ offsets,
-                                                    int32_t *__restrict__ padded,
-                                                    int32_t *__restrict__ tile_expert,
-                                                    int32_t *__restrict__ pair_start,
-                                                    int32_t *__restrict__ pair_expert,
-                                                    const float *__restrict__ prob_part,
-                                                    float *__restrict__ aux, int T, int k) {
+// The scan of one block of 1024 threads (the scan kernel's, or the fused route kernel's
+// last block's). hist and prob_part are read through L2 (.cg): in the fused kernel other
+// blocks wrote them during the same launch.
+__device__ void scan_block(int32_t *__restrict__ hist, int C, int E, int32_t *__restrict__ counts,
+                           int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+                           int32_t *__restrict__ tile_expert, int32_t *__restrict__ pair_start,
+                           int32_t *__restrict__ pair_expert, const float *__restrict__ prob_part,
+                           float *__restrict__ aux, int T, int k) {
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ float s_p[kMaxE];
   __shared__ int32_t s_pad[kMaxE + 1];
@@ -195,7 +220,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
     const int e = warp + 32 * (it / ngroups), c0 = (it % ngroups) * kGroup + kPer * lane;
     const int32_t *h = hist + (int64_t)e * C;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) dst[u] = (c0 + u < C) ? h[c0 + u] : 0;
+    for (int u = 0; u < kPer; ++u) dst[u] = (c0 + u < C) ? __ldcg(h + c0 + u) : 0;
   };
   if (items > 0) load(0, v);
   int32_t running = 0;
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
   if (prob_part) {
     for (int e = warp; e < E; e += 32) {
       float acc = 0.f;  // lane-strided chunks, then a fixed butterfly: a fixed order
-      for (int c = lane; c < C; c += 32) acc += prob_part[(int64_t)e * C + c];
+      for (int c = lane; c < C; c += 32) acc += __ldcg(prob_part + (int64_t)e * C + c);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (lane == 0) s_p[e] = acc / (float)T;
@@ -250,6 +275,19 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, 
     aux[2 * E] = (float)E * l;
   }
   plan_from_counts(s_cnt, E, offsets, padded, tile_expert, pair_start, pair_expert, s_pad, s_pair);
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t *__restrict__ hist, int C, int E,
+                                                    int32_t *__restrict__ counts,
+                                                    int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ padded,
+                                                    int32_t *__restrict__ tile_expert,
+                                                    int32_t *__restrict__ pair_start,
+                                                    int32_t *__restrict__ pair_expert,
+                                                    const float *__restrict__ prob_part,
+                                                    float *__restrict__ aux, int T, int k) {
+  scan_block(hist, C, E, counts, offsets, padded, tile_expert, pair_start, pair_expert, prob_part,
+             aux, T, k);
 }
 
 // The same plan from counts alone (standalone expert FFN calls).
@@ -563,11 +601,11 @@ cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, f
   do {                                                                                     \
     launch_begin(st);                                                                      \
     if (with_count)                                                                        \
-      route_kernel<true, Q><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,          \
-                                                prob_part, T, E, k, C);                    \
+      route_kernel<true, Q, false><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,   \
+                                                       prob_part, T, E, k, C, ScanOut{});  \
     else                                                                                   \
-      route_kernel<false, Q><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,         \
-                                                 prob_part, T, E, k, C);                   \
+      route_kernel<false, Q, false><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,  \
+                                                        prob_part, T, E, k, C, ScanOut{}); \
     return note_launch(with_count ? "route_count" : "route", st);                         \
   } while (0)
   if (E <= 32) MOE_ROUTE(1);
@@ -575,6 +613,27 @@ cudaError_t launch_route(const float *logits, const float *bias, int32_t *ids, f
   if (E <= 128) MOE_ROUTE(4);
   MOE_ROUTE(8);
 #undef MOE_ROUTE
+}
+
+cudaError_t launch_route_count_scan(const float *logits, const float *bias, int32_t *ids,
+                                   float *w, int32_t *rank, int32_t *hist, float *prob_part,
+                                   int T, int E, int k, const ScanOut &so, cudaStream_t st) {
+  const int C = ceil_div(T, kChunk);
+  if (C == 0)  // no token: the scan alone writes the empty plan
+    return launch_scan(hist, T, E, k, so.counts, so.offsets, so.padded, so.tile_expert,
+                       so.pair_start, so.pair_expert, prob_part, so.aux, st);
+#define MOE_ROUTE_SCAN(Q)                                                                   \
+  do {                                                                                     \
+    launch_begin(st);                                                                      \
+    route_kernel<true, Q, true><<<C, 1024, 0, st>>>(logits, bias, ids, w, rank, hist,      \
+                                                    prob_part, T, E, k, C, so);            \
+    return note_launch("route_count_scan", st);                                           \
+  } while (0)
+  if (E <= 32) MOE_ROUTE_SCAN(1);
+  if (E <= 64) MOE_ROUTE_SCAN(2);
+  if (E <= 128) MOE_ROUTE_SCAN(4);
+  MOE_ROUTE_SCAN(8);
+#undef MOE_ROUTE_SCAN
 }
 
 cudaError_t launch_aux_grad(const float *logits, const int32_t *counts, float coeff,
