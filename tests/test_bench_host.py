@@ -41,3 +41,12 @@ def test_kernel_work_flops_sum_to_the_block():
     gemm = sum(v for k, (kind, v) in work.items() if kind == "flop")
     assert gemm == wl.gemm_flops(backward=True)          # 18 A d f
     assert work["router_route_count"] == ("alu_flop", 2 * wl.T * wl.E * wl.d)
+
+
+def test_fused_route_scan_moves_the_bytes_of_both_stages():
+    """The forward's route launch runs the scan in its last block: its algorithmic bytes
+    are those of route + count plus those of the scan."""
+    wl = workloads.WORKLOADS["qwen3_moe"]
+    work = bench.kernel_work(wl)
+    assert work["route_count_scan"][0] == "byte"
+    assert work["route_count_scan"][1] == work["route_count"][1] + work["scan"][1]
